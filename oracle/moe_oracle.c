@@ -1,0 +1,245 @@
+/*
+ * CPU oracle for the small-M MoE decode layer. TEST INFRASTRUCTURE ONLY:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use
+ * it; the CUDA library never links or calls it. Plain loops, no SIMD
+ * intrinsics, no fast-math; built with -ffp-contract=off so that x86 and Arm
+ * hosts give the same bits.
+ *
+ * Every function follows the definitions stated in moe_oracle.h; the
+ * citations below name the page and section each step comes from.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+float oracle_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* e2m1 (FP4): 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit. Exponent
+ * field 0 is subnormal: value = mantissa * 0.5. Otherwise value =
+ * 2^(exp-1) * (1 + mantissa/2). This is the element format of MXFP4 named in
+ * "3 ways to boost MoE inference on NVIDIA DGX Spark", Optimization 1. */
+static double e2m1_magnitude(unsigned code) {
+    unsigned e = (code >> 1) & 3u, m = code & 1u;
+    if (e == 0) return 0.5 * (double)m;
+    return ldexp(1.0 + 0.5 * (double)m, (int)e - 1);
+}
+
+float oracle_mxfp4_value(uint8_t code, uint8_t scale) {
+    if (scale == 255) return NAN; /* e8m0 NaN encoding */
+    double mag = e2m1_magnitude(code & 7u);
+    double v = ldexp(mag, (int)scale - 127);
+    return (float)((code & 8u) ? -v : v);
+}
+
+int oracle_mxfp4_decode(const uint8_t* codes, const uint8_t* scales,
+                        int64_t rows, int K, float* out) {
+    if (!codes || !scales || !out || rows < 0 || K <= 0 || K % 32) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int c = 0; c < K; ++c) {
+            uint8_t byte = codes[r * (K / 2) + c / 2];
+            uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
+            out[r * K + c] = oracle_mxfp4_value(code, scales[r * (K / 32) + c / 32]);
+        }
+    }
+    return 0;
+}
+
+/* One weight element as fp32: bf16 row-major, or MXFP4 codes + scales. */
+static float weight_at(const void* W, const uint8_t* S, int wfmt, int K,
+                       int64_t row, int col) {
+    if (wfmt == 0) return oracle_bf16_to_f32(((const uint16_t*)W)[row * K + col]);
+    const uint8_t* q = (const uint8_t*)W;
+    uint8_t byte = q[row * (K / 2) + col / 2];
+    uint8_t code = (col & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
+    return oracle_mxfp4_value(code, S[row * (K / 32) + col / 32]);
+}
+
+/* Router gate, softmax, top-k, renormalisation.
+ * "Chasing the Batch-1 Floor", section "PDL: stacking the latency floors of
+ * small kernels" (router chain: gate matvec, then top-k) and section "bf16
+ * router gate and lm_head" (bf16 gate weight). Softmax over all experts and
+ * renormalisation of the k selected probabilities is the plain reading of
+ * "routes each token to eight of 512 routed experts" ("3 ways to boost MoE
+ * inference", section "Model and baseline configuration"). */
+int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
+                 int k, int acc_double, float* logits, int32_t* idx, float* w) {
+    if (!x || !Wg || !idx || !w || M < 0 || H <= 0 || E <= 0 || k <= 0 || k > E)
+        return -1;
+    double* l = (double*)malloc(sizeof(double) * (size_t)E);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!l || !p || !taken) { free(l); free(p); free(taken); return -2; }
+    for (int t = 0; t < M; ++t) {
+        const uint16_t* xt = x + (int64_t)t * H;
+        /* step 1: logits, accumulated in index order */
+        for (int e = 0; e < E; ++e) {
+            const uint16_t* we = Wg + (int64_t)e * H;
+            if (acc_double) {
+                double s = 0.0;
+                for (int h = 0; h < H; ++h)
+                    s += (double)oracle_bf16_to_f32(xt[h]) * (double)oracle_bf16_to_f32(we[h]);
+                l[e] = s;
+            } else {
+                float s = 0.0f;
+                for (int h = 0; h < H; ++h) {
+                    float prod = oracle_bf16_to_f32(xt[h]) * oracle_bf16_to_f32(we[h]);
+                    s = s + prod;
+                }
+                l[e] = (double)s;
+            }
+            if (logits) logits[(int64_t)t * E + e] = (float)l[e];
+        }
+        /* step 2: softmax over all E (max-subtracted) */
+        double mx = l[0];
+        for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
+        if (acc_double) {
+            double den = 0.0;
+            for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); den += p[e]; }
+            for (int e = 0; e < E; ++e) p[e] /= den;
+        } else {
+            float den = 0.0f;
+            for (int e = 0; e < E; ++e) {
+                float pe = expf((float)l[e] - (float)mx);
+                p[e] = (double)pe;
+                den = den + pe;
+            }
+            for (int e = 0; e < E; ++e) p[e] = (double)((float)p[e] / den);
+        }
+        /* step 3: the k largest logits; ties go to the lower index. Softmax
+         * is monotone, so ranking logits ranks probabilities. */
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;
+            }
+            taken[best] = 1;
+            idx[(int64_t)t * k + j] = best;
+        }
+        /* step 4: renormalise the selected probabilities */
+        if (acc_double) {
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) s += p[idx[(int64_t)t * k + j]];
+            for (int j = 0; j < k; ++j)
+                w[(int64_t)t * k + j] = (float)(p[idx[(int64_t)t * k + j]] / s);
+        } else {
+            float s = 0.0f;
+            for (int j = 0; j < k; ++j) s = s + (float)p[idx[(int64_t)t * k + j]];
+            for (int j = 0; j < k; ++j)
+                w[(int64_t)t * k + j] = (float)p[idx[(int64_t)t * k + j]] / s;
+        }
+    }
+    free(l); free(p); free(taken);
+    return 0;
+}
+
+/* One SwiGLU expert: g = W1 x, u = W3 x, h = silu(g) * u with
+ * silu(g) = g / (1 + e^-g), computed in fp32 with no intermediate bf16
+ * rounding; z = W2 h. "Chasing the Batch-1 Floor", section "Two fusions and a
+ * retune" (silu(gate) * up in the up-GEMM epilogue, activation kept in float
+ * before the multiply). */
+int oracle_expert(const float* x, int H, int I, int wfmt,
+                  const void* W1, const uint8_t* s1,
+                  const void* W3, const uint8_t* s3,
+                  const void* W2, const uint8_t* s2,
+                  int acc_double, float* z) {
+    if (!x || !W1 || !W3 || !W2 || !z || H <= 0 || I <= 0) return -1;
+    if (wfmt == 1 && (!s1 || !s3 || !s2 || H % 32 || I % 32)) return -1;
+    if (wfmt != 0 && wfmt != 1) return -1;
+    double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+    if (!hd) return -2;
+    for (int i = 0; i < I; ++i) {
+        if (acc_double) {
+            double g = 0.0, u = 0.0;
+            for (int c = 0; c < H; ++c) {
+                g += (double)weight_at(W1, s1, wfmt, H, i, c) * (double)x[c];
+                u += (double)weight_at(W3, s3, wfmt, H, i, c) * (double)x[c];
+            }
+            hd[i] = g / (1.0 + exp(-g)) * u;
+        } else {
+            float g = 0.0f, u = 0.0f;
+            for (int c = 0; c < H; ++c) {
+                float pg = weight_at(W1, s1, wfmt, H, i, c) * x[c];
+                float pu = weight_at(W3, s3, wfmt, H, i, c) * x[c];
+                g = g + pg;
+                u = u + pu;
+            }
+            float sg = g / (1.0f + expf(-g));
+            hd[i] = (double)(sg * u);
+        }
+    }
+    for (int o = 0; o < H; ++o) {
+        if (acc_double) {
+            double s = 0.0;
+            for (int i = 0; i < I; ++i) s += (double)weight_at(W2, s2, wfmt, I, o, i) * hd[i];
+            z[o] = (float)s;
+        } else {
+            float s = 0.0f;
+            for (int i = 0; i < I; ++i) {
+                float prod = weight_at(W2, s2, wfmt, I, o, i) * (float)hd[i];
+                s = s + prod;
+            }
+            z[o] = s;
+        }
+    }
+    free(hd);
+    return 0;
+}
+
+/* Weighted combine of the selected experts plus the always-on shared expert,
+ * summed in fp32 with no intermediate rounding ("Chasing the Batch-1 Floor",
+ * section "PDL: stacking the latency floors of small kernels": fp32 sum with a
+ * single final cast; "3 ways to boost MoE inference", section "Model and
+ * baseline configuration": one shared expert). */
+int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
+               const float* w, int k, int E, int I, int wfmt,
+               const void* const* W1, const uint8_t* const* S1,
+               const void* const* W3, const uint8_t* const* S3,
+               const void* const* W2, const uint8_t* const* S2,
+               int Is, const uint16_t* Ws1, const uint16_t* Ws3,
+               const uint16_t* Ws2, int acc_double, float* y) {
+    if (!x || !y || M < 0 || H <= 0 || k < 0 || E <= 0 || I <= 0 || Is < 0) return -1;
+    if (k > 0 && (!idx || !w || !W1 || !W3 || !W2)) return -1;
+    if (wfmt == 1 && k > 0 && (!S1 || !S3 || !S2)) return -1;
+    if (Is > 0 && (!Ws1 || !Ws3 || !Ws2)) return -1;
+    float* xt = (float*)malloc(sizeof(float) * (size_t)H);
+    float* z = (float*)malloc(sizeof(float) * (size_t)H);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!xt || !z || !acc) { free(xt); free(z); free(acc); return -2; }
+    int rc = 0;
+    for (int t = 0; t < M && rc == 0; ++t) {
+        for (int c = 0; c < H; ++c) xt[c] = oracle_bf16_to_f32(x[(int64_t)t * H + c]);
+        for (int c = 0; c < H; ++c) acc[c] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int e = idx[(int64_t)t * k + j];
+            if (e < 0 || e >= E || !W1[e] || !W3[e] || !W2[e]) { rc = -3; break; }
+            const uint8_t *a = NULL, *b = NULL, *d = NULL;
+            if (wfmt == 1) { a = S1[e]; b = S3[e]; d = S2[e]; }
+            rc = oracle_expert(xt, H, I, wfmt, W1[e], a, W3[e], b, W2[e], d, acc_double, z);
+            if (rc) break;
+            float wj = w[(int64_t)t * k + j];
+            for (int c = 0; c < H; ++c) {
+                if (acc_double) acc[c] += (double)wj * (double)z[c];
+                else acc[c] = (double)((float)acc[c] + wj * z[c]);
+            }
+        }
+        if (rc == 0 && Is > 0) {
+            rc = oracle_expert(xt, H, Is, 0, Ws1, NULL, Ws3, NULL, Ws2, NULL, acc_double, z);
+            for (int c = 0; c < H && rc == 0; ++c) {
+                if (acc_double) acc[c] += (double)z[c];
+                else acc[c] = (double)((float)acc[c] + z[c]);
+            }
+        }
+        for (int c = 0; c < H; ++c) y[(int64_t)t * H + c] = (float)acc[c];
+    }
+    free(xt); free(z); free(acc);
+    return rc;
+}
