@@ -1,0 +1,173 @@
+/*
+ * moe_decode.h - C ABI of the GB300 small-M MoE decode layer library
+ * (libmoe_decode.so, sm_103a).
+ *
+ * The layer, for M = 1..16 tokens (batch-1 decode and speculative verify):
+ *   logits = x Wg^T                      router gate matvec, bf16 weight
+ *   p = softmax(logits); S = top-k(p); w = p_S / sum p_S
+ *   y_t = sum_j w_tj * E_{S_tj}(x_t) + E_shared(x_t)
+ *   E(x) = W2 (silu(W1 x) * (W3 x)),   silu(g) = g / (1 + e^-g)
+ * "Chasing the Batch-1 Floor: Ling-3.0-flash Speculative Decode on
+ * Blackwell" (lmsys.org): sections "The model" (512-expert MoE), "PDL:
+ * stacking the latency floors of small kernels" (router chain norm -> gate
+ * matvec -> top-k; MoE chain up-GEMM -> activation -> down-GEMM -> combine;
+ * fp32 combine with one final cast), "Two fusions and a retune" (SwiGLU in
+ * the up-GEMM epilogue), "bf16 router gate and lm_head"; "3 ways to boost MoE
+ * inference on NVIDIA DGX Spark": "Model and baseline configuration" (8 of 512
+ * routed experts plus one shared expert, hidden 2560) and "Optimization 1"
+ * (MXFP4 expert weights).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must be device (HBM) memory owned by
+ *    the caller, 16-byte aligned. The library allocates and frees nothing.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and never synchronise, except moe_read_status.
+ *  - Return value: MOE_OK (0), or a negative MOE_E* code. A negative code
+ *    from argument checking means nothing was launched. MOE_ECUDA means a
+ *    CUDA call failed (cudaGetLastError is then cleared).
+ *  - Conditions found on the device (an expert index out of range passed to
+ *    moe_ffn, a bounded wait that ran out) do not fault: they are written to
+ *    a status word inside the workspace; read it with moe_read_status.
+ *  - A workspace (`ws`, `ws_bytes` >= moe_workspace_bytes(shape, M)) holds
+ *    the router logits, the SwiGLU activations and the grid-barrier counters.
+ *    Zero it once with moe_workspace_init before its first use; every call
+ *    leaves the counters zeroed again. Calls that share a workspace must be
+ *    ordered on one stream (or otherwise serialised).
+ *
+ * Layouts (row-major; nn.Linear [out, in], contiguous along the reduction
+ * dimension):
+ *   x      bf16 [M, H]           the (already normalised) layer input
+ *   Wg     bf16 [E, H]
+ *   w1, w3 bf16 [E, I, H]        gate and up projections of routed experts
+ *   w2     bf16 [E, H, I]        down projections
+ *   MXFP4 routed experts (wfmt = 1): w1, w3 u8 [E, I, H/2], s1, s3 u8
+ *     [E, I, H/32]; w2 u8 [E, H, I/2], s2 u8 [E, H, I/32]. Codes are e2m1,
+ *     element 2j in the low nibble of byte j; scales are e8m0 (2^(s-127)),
+ *     one per 32 consecutive elements of a row.
+ *   ws1, ws3 bf16 [Is, H]; ws2 bf16 [H, Is]   shared expert (always bf16)
+ *   idx    int32 [M, k]  selected experts, by descending logit (ties: lower
+ *                        index first)
+ *   w      fp32  [M, k]  renormalised routing weights, same order
+ *   y      bf16  [M, H]
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes */
+#define MOE_OK 0
+#define MOE_EINVAL (-1)      /* null pointer or unknown flag/option */
+#define MOE_ESHAPE (-2)      /* shape outside what the kernels support */
+#define MOE_EM (-3)          /* M outside [1, 16] */
+#define MOE_EWORKSPACE (-4)  /* workspace missing or smaller than required */
+#define MOE_EALIGN (-5)      /* a pointer is not 16-byte aligned */
+#define MOE_ECUDA (-6)       /* a CUDA runtime call failed */
+#define MOE_ENODEVICE (-7)   /* no usable CUDA device */
+/* written by the device into the workspace status word */
+#define MOE_EDEVICE_BAD_INDEX (-100) /* moe_ffn got an index outside [0, E);
+                                        that (token, slot) was skipped */
+#define MOE_ETIMEOUT (-101)          /* a bounded device wait ran out; the
+                                        call's outputs are incomplete and the
+                                        workspace must be re-initialised */
+
+/* flags of moe_decode_layer */
+#define MOE_F_NO_PDL 1u                /* launch without programmatic
+                                          dependent launch */
+#define MOE_F_DEBUG_FORCE_TIMEOUT 256u /* test hook: the first grid barrier
+                                          waits for one CTA more than exists,
+                                          so it runs out and reports
+                                          MOE_ETIMEOUT */
+
+/* options of moe_set_option */
+#define MOE_OPT_GRID_CTAS 1       /* CTAs of the persistent grid; 0 = one per
+                                     SM (default). Values above the SM count
+                                     are rejected. */
+#define MOE_OPT_WAIT_TIMEOUT_NS 2 /* budget of each bounded device wait in
+                                     ns (default 1e9) */
+
+typedef struct moe_shape {
+    int32_t hidden;       /* H: multiple of 256 (bf16) or 512 (MXFP4), <= 8192 */
+    int32_t n_experts;    /* E: 1..1024 */
+    int32_t top_k;        /* k: 1..min(16, E) */
+    int32_t inter;        /* I: multiple of 64, at most 4096 */
+    int32_t shared_inter; /* Is: 0 (no shared expert) or a multiple of 64, <= 4096 */
+    int32_t wfmt;         /* routed expert weights: 0 = bf16, 1 = MXFP4 */
+} moe_shape;
+
+typedef struct moe_weights {
+    const void* w1;     /* routed gate projection  (device) */
+    const void* w3;     /* routed up projection    (device) */
+    const void* w2;     /* routed down projection  (device) */
+    const uint8_t* s1;  /* MXFP4 scales of w1, w3, w2; NULL for bf16 */
+    const uint8_t* s3;
+    const uint8_t* s2;
+    const void* ws1;    /* shared expert, bf16; NULL when Is == 0 */
+    const void* ws3;
+    const void* ws2;
+} moe_weights;
+
+/* Bytes of workspace a call with this shape and M needs. 0 for a shape or M
+ * the library rejects. */
+size_t moe_workspace_bytes(const moe_shape* shape, int M);
+
+/* Zeroes the workspace (device, ws_bytes) on `stream`; needed once before
+ * the first call and after a call reported MOE_ETIMEOUT. */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Router alone: logits = x Wg^T in fp32, softmax, top-k, renormalised
+ * weights. x bf16 [M,H], Wg bf16 [E,H] (device); idx int32 [M,k] and
+ * w fp32 [M,k] (device) receive the routing. */
+int moe_route(const void* x, int M, const void* Wg, const moe_shape* shape,
+              int32_t* idx, float* w, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert FFN with the routing given: y = sum_j w[t,j] E_{idx[t,j]}(x_t)
+ * + E_shared(x_t), gate/up + SwiGLU + down + combine; each touched expert's
+ * weights are read from HBM once whatever M is. idx/w (device) as returned
+ * by moe_route; an idx entry may repeat within a token (its weights then
+ * add). An entry outside [0, E) is skipped and reported through the status
+ * word. y bf16 [M,H] (device). */
+int moe_ffn(const void* x, int M, const int32_t* idx, const float* w,
+            const moe_weights* weights, const moe_shape* shape, void* y,
+            void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer in one persistent launch: router, top-k, gate/up +
+ * SwiGLU, down + combine, shared expert. idx_out / w_out (device) may be
+ * NULL. y bf16 [M,H] (device). flags: MOE_F_*. The result is deterministic:
+ * every output element is accumulated in a fixed order, so it does not
+ * depend on scheduling, PDL or the run. */
+int moe_decode_layer(const void* x, int M, const void* Wg,
+                     const moe_weights* weights, const moe_shape* shape,
+                     int32_t* idx_out, float* w_out, void* y, void* ws,
+                     size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Synchronises `stream`, then copies the device status word of `ws` to
+ * *dev_status (MOE_OK or a device code above). Not for the hot path. */
+int moe_read_status(const void* ws, void* stream, int32_t* dev_status);
+
+/* Static description of a MOE_* code. */
+const char* moe_status_str(int code);
+
+/* Dequantises MXFP4 rows with the decode the kernels use: out fp32
+ * [rows, K] = e2m1(code) * 2^(scale - 127). codes u8 [rows, K/2], scales
+ * u8 [rows, K/32], out (all device); K a multiple of 32. */
+int moe_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales,
+                      int64_t rows, int K, float* out, void* stream);
+
+/* Process-wide tuning and test options (MOE_OPT_*). Not thread-safe with
+ * concurrent calls. */
+int moe_set_option(int option, int64_t value);
+
+/* Number of kernel launches the most recent call on this thread made
+ * (1 for moe_decode_layer / moe_route / moe_ffn). */
+int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,12 @@
+// Host-side launch entry points of the layer kernel (one per weight format).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "layer_params.h"
+
+namespace moe {
+cudaError_t launch_layer_bf16(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
+cudaError_t launch_layer_mxfp4(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
+cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, float* out,
+                                 cudaStream_t stream);
+}  // namespace moe

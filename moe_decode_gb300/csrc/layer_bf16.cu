@@ -1,0 +1,10 @@
+// bf16 routed experts: instantiation and launch of the persistent layer kernel.
+#include "launch.h"
+#include "launch_common.cuh"
+#include "layer_kernel.cuh"
+
+namespace moe {
+cudaError_t launch_layer_bf16(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
+    return launch_persistent(moe_layer_kernel<0>, p, stream, pdl, coop);
+}
+}  // namespace moe

@@ -1,0 +1,75 @@
+// Launch parameters shared by the host launcher and the persistent layer
+// kernel. Plain C++ (no CUDA types), included by both sides.
+#pragma once
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr uint32_t kStageBytes = 32768;               // one ring stage
+constexpr int kMaxStages = 6;
+constexpr int kMaxM = 16;
+constexpr int kMaxK = 16;
+constexpr int kMaxE = 1024;
+constexpr int kMaxEntries = kMaxM * kMaxK;
+
+// workspace control block (uint32 words; counters 128 bytes apart)
+constexpr int kCtlStatus = 0;
+constexpr int kCtlBar1 = 32;
+constexpr int kCtlBar2 = 64;
+constexpr int kCtlExit = 96;
+constexpr uint32_t kCtlBytes = 1024;
+
+enum : int { kModeRoute = 1, kModeFfn = 2, kModeLayer = 3 };
+
+struct LayerParams {
+    const uint16_t* x;     // [M, H] bf16
+    const uint16_t* Wg;    // [E, H] bf16
+    const uint8_t* w1;     // routed weights (bf16 or MXFP4 codes), bytes
+    const uint8_t* w3;
+    const uint8_t* w2;
+    const uint8_t* s1;     // MXFP4 scales
+    const uint8_t* s3;
+    const uint8_t* s2;
+    const uint16_t* ws1;   // shared expert, bf16
+    const uint16_t* ws3;
+    const uint16_t* ws2;
+    const int32_t* idx_in; // FFN mode routing
+    const float* w_in;
+    int32_t* idx_out;      // may be null
+    float* w_out;
+    uint16_t* y;           // [M, H] bf16
+    unsigned* ctrl;        // workspace control block
+    float* logits;         // [M, E]
+    uint16_t* hs;          // shared-expert activations [M, Is] bf16
+    uint16_t* hr;          // routed activations [M*k, I] bf16, grouped by expert
+    int M, H, E, k, I, Is;
+    int mode;
+    int G;                 // CTAs in the grid
+    int ns;                // ring stages
+    int rpc;               // rows of y owned per CTA, upper bound (ceil(H/G))
+    int force_timeout;
+    unsigned long long timeout_ns;
+    uint32_t off_bar, off_plan, off_x, off_yacc, smem_bytes;
+};
+
+// Expert plan, rebuilt by every CTA after routing.
+struct Plan {
+    int32_t sel_e[kMaxEntries];   // routing, token-major [M][k]
+    float sel_w[kMaxEntries];
+    int32_t rank[kMaxEntries];
+    int32_t first[kMaxEntries];
+    int16_t pair_tok[kMaxEntries];  // routed (token, weight) pairs grouped by expert
+    float pair_w[kMaxEntries];
+    int16_t slot_e[kMaxEntries];    // distinct routed experts, ascending
+    int16_t slot_p0[kMaxEntries + 1];
+    int32_t nslot;
+    int32_t npairs;
+    int32_t abort;
+    int32_t pad;
+};
+
+
+}  // namespace moe

@@ -224,3 +224,41 @@ def x_overlap(shape: LayerShape, step: int, M: int, rho: float = RHO_OVERLAP_M10
     a = u * c1
     b = z * c2
     return (a + b).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# whole layers on the device
+
+def device_layer(shape: LayerShape, copy: int, wfmt: int = 0, device="cuda") -> dict:
+    """All weights of layer copy `copy`, generated on `device`.
+
+    Keys: Wg, ws1, ws3, ws2 (bf16) and, for wfmt 0, w1, w3, w2 (bf16
+    [E,I,H], [E,I,H], [E,H,I]); for wfmt 1, w1, w3, w2 as MXFP4 codes with
+    s1, s3, s2 scales (the bf16 draws quantised, expert block by block)."""
+    d = {"Wg": router_weight(shape, copy, device)}
+    d["ws1"], d["ws3"], d["ws2"] = shared_weights(shape, copy, device)
+    E, H, I = shape.n_experts, shape.hidden, shape.inter
+    seed = LAYER_SEED0 + copy
+    n = I * H
+    if wfmt == 0:
+        d["w1"], d["w3"], d["w2"] = all_expert_weights(shape, copy, device)
+        return d
+    blk = max(1, (1 << 24) // n)
+    for name, tid, rows, K in (("w1", T_W1, I, H), ("w3", T_W3, I, H), ("w2", T_W2, H, I)):
+        codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty((E, rows, K // 32), dtype=torch.uint8, device=device)
+        for e0 in range(0, E, blk):
+            e1 = min(E, e0 + blk)
+            w = normal_bf16(seed, tid, e0 * n, (e1 - e0) * n, WEIGHT_SIGMA, device).view(e1 - e0, rows, K)
+            codes[e0:e1], scales[e0:e1] = mxfp4_quantize(w)
+        d[name] = codes
+        d["s" + name[1]] = scales
+    return d
+
+
+def host_expert(shape: LayerShape, layer: dict, e: int, wfmt: int = 0):
+    """Host (numpy) copies of expert e's weights from a device layer, in the
+    tuple order the CPU oracle takes."""
+    if wfmt == 0:
+        return tuple(to_u16(layer[n][e]) for n in ("w1", "w3", "w2"))
+    return tuple(layer[n][e].cpu().numpy() for n in ("w1", "s1", "w3", "s3", "w2", "s2"))
