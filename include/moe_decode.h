@@ -90,6 +90,11 @@ extern "C" {
                                      are rejected. */
 #define MOE_OPT_WAIT_TIMEOUT_NS 2 /* budget of each bounded device wait in
                                      ns (default 1e9) */
+#define MOE_OPT_TRACE_BUFFER 3    /* diagnostic: device address of a uint64
+                                     buffer of at least 16 x (grid CTAs)
+                                     entries; each CTA writes the global timer
+                                     (ns) at its phase boundaries into its 16
+                                     entries. 0 (default) disables it. */
 
 typedef struct moe_shape {
     int32_t hidden;       /* H: multiple of 256 (bf16) or 512 (MXFP4), <= 8192 */
@@ -163,8 +168,8 @@ int moe_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales,
  * concurrent calls. */
 int moe_set_option(int option, int64_t value);
 
-/* Number of kernel launches the most recent call on this thread made
- * (1 for moe_decode_layer / moe_route / moe_ffn). */
+/* Number of kernel launches the most recent launching call on this thread
+ * made (1 for moe_decode_layer / moe_route / moe_ffn). */
 int moe_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -25,6 +25,7 @@ F_NO_PDL = 1
 F_DEBUG_FORCE_TIMEOUT = 256
 OPT_GRID_CTAS = 1
 OPT_WAIT_TIMEOUT_NS = 2
+OPT_TRACE_BUFFER = 3
 
 
 class MoeError(RuntimeError):

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/moe_decode.h"
+#include "moe_decode.h"
 #include "launch.h"
 #include "layer_params.h"
 
@@ -17,6 +17,7 @@ using moe::LayerParams;
 struct Options {
     int grid_ctas = 0;
     long long timeout_ns = 1000000000LL;
+    unsigned long long* trace = nullptr;
 };
 Options g_opt;
 thread_local int g_last_launches = 0;
@@ -108,6 +109,7 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.G = G;
     p.rpc = (p.H + G - 1) / G;
     p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
+    p.trace = g_opt.trace;
     uint8_t* base = static_cast<uint8_t*>(ws);
     p.ctrl = reinterpret_cast<unsigned*>(base);
     p.logits = reinterpret_cast<float*>(base + wl.logits);
@@ -184,7 +186,6 @@ size_t moe_workspace_bytes(const moe_shape* shape, int M) {
 }
 
 int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
-    g_last_launches = 0;
     if (!ws) return MOE_EINVAL;
     if (ws_bytes < moe::kCtlBytes) return MOE_EWORKSPACE;
     if (cudaMemsetAsync(ws, 0, moe::kCtlBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
@@ -255,7 +256,6 @@ int moe_decode_layer(const void* x, int M, const void* Wg, const moe_weights* we
 }
 
 int moe_read_status(const void* ws, void* stream, int32_t* dev_status) {
-    g_last_launches = 0;
     if (!ws || !dev_status) return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t v = 0;
@@ -306,6 +306,10 @@ int moe_set_option(int option, int64_t value) {
         case MOE_OPT_WAIT_TIMEOUT_NS:
             if (value <= 0) return MOE_EINVAL;
             g_opt.timeout_ns = value;
+            return MOE_OK;
+        case MOE_OPT_TRACE_BUFFER:
+            if (value < 0 || (value & 7)) return MOE_EINVAL;
+            g_opt.trace = reinterpret_cast<unsigned long long*>(value);
             return MOE_OK;
         default: return MOE_EINVAL;
     }

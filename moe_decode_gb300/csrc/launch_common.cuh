@@ -7,12 +7,13 @@
 namespace moe {
 
 template <class Kernel>
-cudaError_t launch_persistent(Kernel kernel, const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
+cudaError_t launch_persistent(Kernel kernel, int threads, const LayerParams& p, cudaStream_t stream, bool pdl,
+                              bool coop) {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.G, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = p.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];

@@ -5,6 +5,6 @@
 
 namespace moe {
 cudaError_t launch_layer_bf16(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
-    return launch_persistent(moe_layer_kernel<0>, p, stream, pdl, coop);
+    return launch_persistent(moe_layer_kernel<0>, block_threads(0), p, stream, pdl, coop);
 }
 }  // namespace moe

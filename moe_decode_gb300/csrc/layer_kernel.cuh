@@ -41,10 +41,10 @@
 
 namespace moe {
 
-constexpr int NCW = kConsumerWarps;
-constexpr int NCT = kConsumerThreads;
 constexpr uint32_t SB = kStageBytes;
-constexpr int TG = 4;  // tokens (pairs) per register group
+// Split a chunk's rows along K over all consumer warps (off: measured slower
+// than giving each row to one warp, see the split_ns comment).
+constexpr bool kSplitK = false;
 
 // A unit of the ring: the tiles one stage holds.
 struct Chunk {
@@ -95,14 +95,22 @@ __device__ __forceinline__ void for_shared_gateup_chunks(const Ctx& x, F&& f) {
 template <int WFMT, class F>
 __device__ __forceinline__ void for_routed_gateup_chunks(const Ctx& x, F&& f) {
     const LayerParams& p = x.p;
-    long long R = (long long)x.plan->nslot * p.I;
-    long long r = (long long)x.c * R / p.G, r1 = (long long)(x.c + 1) * R / p.G;
-    int cap = gateup_cap<WFMT>(p, true);
+    const uint32_t I = (uint32_t)p.I;
+    const uint32_t R = (uint32_t)x.plan->nslot * I;  // <= 256 * 4096
+    const uint32_t G = (uint32_t)p.G, c = (uint32_t)x.c;
+    uint32_t r = (uint32_t)(((uint64_t)c * R) / G), r1 = (uint32_t)(((uint64_t)(c + 1) * R) / G);
+    const uint32_t cap = (uint32_t)gateup_cap<WFMT>(p, true);
+    if (r >= r1) return;
+    uint32_t s = r / I, i0 = r - s * I;
     while (r < r1) {
-        int s = (int)(r / p.I), i0 = (int)(r % p.I);
-        int n = (int)min((long long)cap, min(r1 - r, (long long)(p.I - i0)));
-        f(Chunk{1, s, i0, n, 0, 0});
+        uint32_t n = min(cap, min(r1 - r, I - i0));
+        f(Chunk{1, (int)s, (int)i0, (int)n, 0, 0});
         r += n;
+        i0 += n;
+        if (i0 == I) {
+            i0 = 0;
+            ++s;
+        }
     }
 }
 
@@ -132,6 +140,13 @@ __device__ __forceinline__ void for_down_chunks(const Ctx& x, F&& f) {
     }
 }
 
+// Optional phase trace: slot i of this CTA's 16-entry record gets the global
+// timer (ns). Slots 0-7 are written by consumer thread 0, 8-15 by the
+// producer lane.
+__device__ __forceinline__ void trace_mark(const LayerParams& p, int slot) {
+    if (p.trace) p.trace[(size_t)blockIdx.x * 16 + slot] = global_timer_ns();
+}
+
 // ------------------------------------------------------------ failure paths
 __device__ __forceinline__ void raise_status(const LayerParams& p, int code) {
     atomicCAS(reinterpret_cast<int*>(p.ctrl + kCtlStatus), 0, code);
@@ -147,6 +162,9 @@ __device__ __forceinline__ bool aborted(const Plan* plan) {
 }
 
 // Bounded mbarrier wait: false when the budget ran out or the CTA aborted.
+// The waiting warp suspends in the barrier probe (it issues nothing while
+// suspended, leaving issue slots and the shared-memory pipe to the warps that
+// compute) and resumes when the phase completes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const LayerParams& p, Plan* plan) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
@@ -224,12 +242,14 @@ struct Producer {
         uint32_t i = ring.n;
         if (i < (uint32_t)ring.ns) return true;
         uint32_t bar = ring.empty(i), par = ring.parity(i) ^ 1u;
-        if (mbar_try_wait(bar, par)) return true;
+        if (mbar_test_wait(bar, par)) return true;
         uint64_t t0 = global_timer_ns();
         while (true) {
-            if (mbar_try_wait(bar, par)) return true;
-            if (aborted(plan)) return false;
+            // suspend for at most ~0.25 us at a time, so that barrier 2 is
+            // polled promptly during phase 2
+            if (mbar_try_wait_hint(bar, par, phase2 ? 256u : 100000u)) return true;
             if (phase2) poll_b2(false);
+            if (aborted(plan)) return false;
             if (global_timer_ns() - t0 > x.p.timeout_ns) {
                 set_abort(x.p, plan, -101);
                 return false;
@@ -330,6 +350,11 @@ struct Producer {
 };
 
 // ------------------------------------------------------------ consumer math
+// Dot products over rows held in shared memory. Lanes stride the row's
+// 16-byte vectors; each token keeps four independent partial sums so that the
+// FMA dependency chains stay short and the loads of several vectors are in
+// flight at once. Token groups are at most two wide (NT), which keeps all
+// accumulators in registers.
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -337,116 +362,123 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// acc[t] += row . xr[t] over nvec 16-byte vectors (bf16 x 8), lanes strided.
-__device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const uint4* const* xr, int cnt, int nvec,
-                                         int lane, float (&acc)[TG]) {
-#pragma unroll 2
-    for (int v = lane; v < nvec; v += 32) {
+template <int NT>
+__device__ __forceinline__ void sum4(const float (&pa)[NT][4], float (&acc)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0] + pa[t][1]) + (pa[t][2] + pa[t][3]);
+}
+
+// acc[t] = row . x_t (bf16 x bf16, fp32 accumulate) over nvec 16-byte
+// vectors; this lane takes vectors lane, lane + STRIDE, ...
+template <int NT, int STRIDE = 32>
+__device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const uint4* __restrict__ x0,
+                                         const uint4* __restrict__ x1, int nvec, int lane, float (&acc)[NT]) {
+    float pa[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += STRIDE) {
         float fw[8];
         unpack8(row[v], fw);
 #pragma unroll
-        for (int t = 0; t < TG; ++t) {
-            if (t < cnt) {
-                float fx[8];
-                unpack8(xr[t][v], fx);
+        for (int t = 0; t < NT; ++t) {
+            float fx[8];
+            unpack8((t == 0 ? x0 : x1)[v], fx);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[t] = fmaf(fw[e], fx[e], acc[t]);
-            }
+            for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
         }
     }
+    sum4<NT>(pa, acc);
 }
 
 // Gate and up rows against the same tokens.
+template <int NT>
 __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const uint4* __restrict__ r3,
-                                          const uint4* const* xr, int cnt, int nvec, int lane, float (&g)[TG],
-                                          float (&u)[TG]) {
-#pragma unroll 2
+                                          const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nvec,
+                                          int lane, float (&g)[NT], float (&u)[NT]) {
+    float pg[NT][4], pu[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) pg[t][0] = pg[t][1] = pg[t][2] = pg[t][3] = pu[t][0] = pu[t][1] = pu[t][2] = pu[t][3] = 0.f;
+#pragma unroll 5
     for (int v = lane; v < nvec; v += 32) {
         float f1[8], f3[8];
         unpack8(r1[v], f1);
         unpack8(r3[v], f3);
 #pragma unroll
-        for (int t = 0; t < TG; ++t) {
-            if (t < cnt) {
-                float fx[8];
-                unpack8(xr[t][v], fx);
+        for (int t = 0; t < NT; ++t) {
+            float fx[8];
+            unpack8((t == 0 ? x0 : x1)[v], fx);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    g[t] = fmaf(f1[e], fx[e], g[t]);
-                    u[t] = fmaf(f3[e], fx[e], u[t]);
-                }
+            for (int e = 0; e < 8; ++e) {
+                pg[t][e & 3] = fmaf(f1[e], fx[e], pg[t][e & 3]);
+                pu[t][e & 3] = fmaf(f3[e], fx[e], pu[t][e & 3]);
             }
         }
     }
+    sum4<NT>(pg, g);
+    sum4<NT>(pu, u);
 }
 
-// MXFP4 rows: 16-byte code blocks of 32 elements with one e8m0 scale each.
+// One 32-element MXFP4 block (16 code bytes) against 32 bf16 values of each
+// token; returns the unscaled block sums.
+template <int NT>
+__device__ __forceinline__ void block_mxfp4(const uint4 q, const uint4* __restrict__ x0, const uint4* __restrict__ x1,
+                                            int b, float (&bs)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) bs[t] = 0.f;
+    float pa[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t a = (&q.x)[w];
+        float d[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[e] = e2m1_to_f32(a >> (4 * e));
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float fx[8];
+            unpack8((t == 0 ? x0 : x1)[b * 4 + w], fx);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(d[e], fx[e], pa[t][e & 3]);
+        }
+    }
+    sum4<NT>(pa, bs);
+}
+
+// MXFP4 gate and up rows: per block, the code sums times the e8m0 scale.
+template <int NT>
 __device__ __forceinline__ void dot2_mxfp4(const uint4* __restrict__ c1, const uint8_t* __restrict__ s1,
                                            const uint4* __restrict__ c3, const uint8_t* __restrict__ s3,
-                                           const uint4* const* xr, int cnt, int nblk, int lane, float (&g)[TG],
-                                           float (&u)[TG]) {
+                                           const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nblk,
+                                           int lane, float (&g)[NT], float (&u)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
     for (int b = lane; b < nblk; b += 32) {
-        const uint4 q1 = c1[b], q3 = c3[b];
-        float bg[TG], bu[TG];
+        float bg[NT], bu[NT];
+        block_mxfp4<NT>(c1[b], x0, x1, b, bg);
+        block_mxfp4<NT>(c3[b], x0, x1, b, bu);
+        const float sc1 = e8m0_to_f32(s1[b]), sc3 = e8m0_to_f32(s3[b]);
 #pragma unroll
-        for (int t = 0; t < TG; ++t) bg[t] = bu[t] = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            uint32_t a = (&q1.x)[w], c = (&q3.x)[w];
-            float d1[8], d3[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                d1[e] = e2m1_to_f32(a >> (4 * e));
-                d3[e] = e2m1_to_f32(c >> (4 * e));
-            }
-#pragma unroll
-            for (int t = 0; t < TG; ++t) {
-                if (t < cnt) {
-                    float fx[8];
-                    unpack8(xr[t][b * 4 + w], fx);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        bg[t] = fmaf(d1[e], fx[e], bg[t]);
-                        bu[t] = fmaf(d3[e], fx[e], bu[t]);
-                    }
-                }
-            }
-        }
-        float sc1 = e8m0_to_f32(s1[b]), sc3 = e8m0_to_f32(s3[b]);
-#pragma unroll
-        for (int t = 0; t < TG; ++t) {
+        for (int t = 0; t < NT; ++t) {
             g[t] = fmaf(bg[t], sc1, g[t]);
             u[t] = fmaf(bu[t], sc3, u[t]);
         }
     }
 }
 
+template <int NT, int STRIDE = 32>
 __device__ __forceinline__ void dot_mxfp4(const uint4* __restrict__ c, const uint8_t* __restrict__ s,
-                                          const uint4* const* hr, int cnt, int nblk, int lane, float (&acc)[TG]) {
-    for (int b = lane; b < nblk; b += 32) {
-        const uint4 q = c[b];
-        float ba[TG];
+                                          const uint4* __restrict__ h0, const uint4* __restrict__ h1, int nblk,
+                                          int lane, float (&acc)[NT]) {
 #pragma unroll
-        for (int t = 0; t < TG; ++t) ba[t] = 0.f;
+    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+    for (int b = lane; b < nblk; b += STRIDE) {
+        float bs[NT];
+        block_mxfp4<NT>(c[b], h0, h1, b, bs);
+        const float sc = e8m0_to_f32(s[b]);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            uint32_t a = (&q.x)[w];
-            float d[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) d[e] = e2m1_to_f32(a >> (4 * e));
-#pragma unroll
-            for (int t = 0; t < TG; ++t) {
-                if (t < cnt) {
-                    float fx[8];
-                    unpack8(hr[t][b * 4 + w], fx);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ba[t] = fmaf(d[e], fx[e], ba[t]);
-                }
-            }
-        }
-        float sc = e8m0_to_f32(s[b]);
-#pragma unroll
-        for (int t = 0; t < TG; ++t) acc[t] = fmaf(ba[t], sc, acc[t]);
+        for (int t = 0; t < NT; ++t) acc[t] = fmaf(bs[t], sc, acc[t]);
     }
 }
 
@@ -455,6 +487,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // ------------------------------------------------------------ consumer
 template <int WFMT>
 struct Consumer {
+    static constexpr int NCW = consumer_warps(WFMT);
     const Ctx& x;
     Ring ring;
     Plan* plan;
@@ -463,43 +496,143 @@ struct Consumer {
     int warp, lane, tid;
     int q;               // running row counter (row ownership)
 
-    __device__ bool wait_full() {
+    __device__ __forceinline__ bool wait_full() {
         return mbar_wait(ring.full(ring.n), ring.parity(ring.n), x.p, plan);
     }
-    __device__ void release() {
+    __device__ __forceinline__ void release() {
         __syncwarp();
         if (lane == 0) mbar_arrive(ring.empty(ring.n));
         ring.n++;
     }
-    __device__ const uint8_t* stage_ptr() const {
+    __device__ __forceinline__ const uint8_t* stage_ptr() const {
         return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(ring.stage(ring.n)));
+    }
+    __device__ __forceinline__ const uint4* xrow(int tok) const {
+        return reinterpret_cast<const uint4*>(xs + (size_t)tok * x.p.H);
+    }
+
+    __device__ __forceinline__ float* part_buf() const { return plan->part[ring.n % ring.ns]; }
+
+    // Split-K layout of a chunk of n rows whose reduction dimension spans ncol
+    // columns of 32 lanes: NS slices per row so that the n * NS units keep
+    // every consumer warp busy. NS = 1 means no split.
+    __device__ __forceinline__ int split_ns(int n, int ncol, int npairs) const {
+        if (!kSplitK || n >= NCW || npairs > kSplitPairs || ncol < 2) return 1;
+        return max(1, min(NCW / n, min(ncol, kSplitUnits / n)));
+    }
+
+    // Called by every consumer warp once per split chunk, after its partial
+    // sums are stored: returns true in the last warp to arrive, which then
+    // sees every warp's partials.
+    __device__ __forceinline__ bool last_to_arrive() const {
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            old = atomicAdd(&plan->arrive[ring.n % ring.ns], 1);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != NCW - 1) return false;
+        __threadfence_block();
+        return true;
+    }
+    __device__ __forceinline__ void reset_arrival() const {
+        __syncwarp();
+        if (lane == 0) plan->arrive[ring.n % ring.ns] = 0;
     }
 
     __device__ bool router(const Chunk& ch) {
         if (!wait_full()) return false;
         const LayerParams& p = x.p;
         const uint8_t* st = stage_ptr();
-        const int nvec = p.H / 8;
-        for (int j = 0; j < ch.n; ++j, ++q) {
-            if (q % NCW != warp) continue;
-            const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
-            for (int t0 = 0; t0 < p.M; t0 += TG) {
-                int cnt = min(TG, p.M - t0);
-                const uint4* xr[TG];
-#pragma unroll
-                for (int t = 0; t < TG; ++t)
-                    xr[t] = reinterpret_cast<const uint4*>(xs + (size_t)min(t0 + t, p.M - 1) * p.H);
-                float acc[TG] = {0.f, 0.f, 0.f, 0.f};
-                dot_bf16(row, xr, cnt, nvec, lane, acc);
-#pragma unroll
-                for (int t = 0; t < TG; ++t) acc[t] = warp_sum(acc[t]);
-#pragma unroll
-                for (int t = 0; t < TG; ++t)
-                    if (t < cnt && lane == t) p.logits[(size_t)(t0 + t) * p.E + ch.r0 + j] = acc[t];
+        const int ncol = p.H / 256;
+        const int NS = split_ns(ch.n, ncol, p.M);
+        if (NS == 1) {
+            for (int j = 0; j < ch.n; ++j, ++q) {
+                if (q % NCW != warp) continue;
+                const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
+                for (int t = 0; t < p.M; ++t) {
+                    float acc[1];
+                    dot_bf16<1>(row, xrow(t), xrow(t), p.H / 8, lane, acc);
+                    acc[0] = warp_sum(acc[0]);
+                    if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
+                }
+            }
+        } else {
+            q += ch.n;
+            const int cs = (ncol + NS - 1) / NS;
+            float* part = part_buf();
+            if (warp < ch.n * NS) {
+                const int j = warp / NS, sl = warp - j * NS;
+                const int c0 = sl * cs, c1 = min(ncol, c0 + cs);
+                const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
+                for (int t = 0; t < p.M; ++t) {
+                    float acc[1];
+                    dot_bf16<1>(row, xrow(t), xrow(t), 32 * c1, lane + 32 * c0, acc);
+                    acc[0] = warp_sum(acc[0]);
+                    if (lane == 0) part[(warp * kSplitPairs + t) * 2] = acc[0];
+                }
+            }
+            if (last_to_arrive()) {
+                for (int it = lane; it < ch.n * p.M; it += 32) {
+                    const int j = it / p.M, t = it - j * p.M;
+                    float v = 0.f;
+                    for (int s2 = 0; s2 < NS; ++s2) v += part[((j * NS + s2) * kSplitPairs + t) * 2];
+                    p.logits[(size_t)t * p.E + ch.r0 + j] = v;
+                }
+                reset_arrival();
             }
         }
         release();
         return true;
+    }
+
+    // Gate/up dot products of row pair j over lane columns [c0, c1) for two
+    // (or one) tokens.
+    template <int NT>
+    __device__ __forceinline__ void gateup_group(const uint8_t* st, const Chunk& ch, int j, int t0tok, int t1tok,
+                                                 bool shared, int c0, int c1, float (&g)[NT], float (&u)[NT]) const {
+        const LayerParams& p = x.p;
+        if (WFMT == 0 || shared) {
+            const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
+            const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
+            dot2_bf16<NT>(r1, r3, xrow(t0tok), xrow(t1tok), min(32 * c1, p.H / 8), lane + 32 * c0, g, u);
+        } else {
+            const size_t cb = (size_t)p.H / 2, sbytes = (size_t)p.H / 32;
+            const uint4* c1p = reinterpret_cast<const uint4*>(st + j * cb);
+            const uint4* c3p = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
+            const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
+            const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
+            dot2_mxfp4<NT>(c1p, s1, c3p, s3, xrow(t0tok), xrow(t1tok), min(32 * c1, p.H / 32), lane + 32 * c0, g, u);
+        }
+    }
+
+    // All tokens of the slot against row pair j over lane columns [c0, c1);
+    // out(pair, g, u) receives the warp-reduced sums (valid in lane 0).
+    template <class Out>
+    __device__ __forceinline__ void gateup_row(const uint8_t* st, const Chunk& ch, int j, bool shared, int npairs,
+                                               int pbase, int c0, int c1, Out&& out) const {
+        int q0 = 0;
+        for (; q0 + 2 <= npairs; q0 += 2) {
+            const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
+            const int tb = shared ? q0 + 1 : plan->pair_tok[pbase + q0 + 1];
+            float g[2], u[2];
+            gateup_group<2>(st, ch, j, ta, tb, shared, c0, c1, g, u);
+            g[0] = warp_sum(g[0]);
+            u[0] = warp_sum(u[0]);
+            g[1] = warp_sum(g[1]);
+            u[1] = warp_sum(u[1]);
+            out(q0, g[0], u[0]);
+            out(q0 + 1, g[1], u[1]);
+        }
+        if (q0 < npairs) {
+            const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
+            float g[1], u[1];
+            gateup_group<1>(st, ch, j, ta, ta, shared, c0, c1, g, u);
+            g[0] = warp_sum(g[0]);
+            u[0] = warp_sum(u[0]);
+            out(q0, g[0], u[0]);
+        }
     }
 
     __device__ bool gateup(const Chunk& ch) {
@@ -510,45 +643,77 @@ struct Consumer {
         const int inter = shared ? p.Is : p.I;
         const int npairs = slot_npairs(x, ch.slot);
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
-        uint16_t* hdst = shared ? p.hs : p.hr;
-        for (int j = 0; j < ch.n; ++j, ++q) {
-            if (q % NCW != warp) continue;
-            const int i = ch.r0 + j;
-            for (int q0 = 0; q0 < npairs; q0 += TG) {
-                int cnt = min(TG, npairs - q0);
-                const uint4* xr[TG];
-#pragma unroll
-                for (int t = 0; t < TG; ++t) {
-                    int pp = min(q0 + t, npairs - 1);
-                    int tok = shared ? pp : plan->pair_tok[pbase + pp];
-                    xr[t] = reinterpret_cast<const uint4*>(xs + (size_t)tok * p.H);
+        uint16_t* hdst = (shared ? p.hs : p.hr) + (size_t)pbase * inter + ch.r0;
+        const int ncol = (WFMT == 0 || shared) ? p.H / 256 : (p.H / 32 + 31) / 32;
+        const int NS = split_ns(ch.n, ncol, npairs);
+        if (NS == 1) {
+            for (int j = 0; j < ch.n; ++j, ++q) {
+                if (q % NCW != warp) continue;
+                gateup_row(st, ch, j, shared, npairs, pbase, 0, ncol, [&](int pr, float g, float u) {
+                    if (lane == 0) hdst[(size_t)pr * inter + j] = f32_to_bf16_bits(silu_mul(g, u));
+                });
+            }
+        } else {
+            q += ch.n;
+            const int cs = (ncol + NS - 1) / NS;
+            float* part = part_buf();
+            if (warp < ch.n * NS) {
+                const int j = warp / NS, sl = warp - j * NS;
+                const int c0 = sl * cs, c1 = min(ncol, c0 + cs);
+                float* mine = part + warp * kSplitPairs * 2;
+                gateup_row(st, ch, j, shared, npairs, pbase, c0, c1, [&](int pr, float g, float u) {
+                    if (lane == 0) {
+                        mine[pr * 2] = g;
+                        mine[pr * 2 + 1] = u;
+                    }
+                });
+            }
+            if (last_to_arrive()) {
+                for (int it = lane; it < ch.n * npairs; it += 32) {
+                    const int j = it / npairs, pr = it - j * npairs;
+                    float g = 0.f, u = 0.f;
+                    for (int s2 = 0; s2 < NS; ++s2) {
+                        const float* src = part + ((j * NS + s2) * kSplitPairs + pr) * 2;
+                        g += src[0];
+                        u += src[1];
+                    }
+                    hdst[(size_t)pr * inter + j] = f32_to_bf16_bits(silu_mul(g, u));
                 }
-                float g[TG] = {0.f, 0.f, 0.f, 0.f}, u[TG] = {0.f, 0.f, 0.f, 0.f};
-                if (WFMT == 0 || shared) {
-                    const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
-                    const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
-                    dot2_bf16(r1, r3, xr, cnt, p.H / 8, lane, g, u);
-                } else {
-                    const size_t cb = (size_t)p.H / 2, sbytes = (size_t)p.H / 32;
-                    const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
-                    const uint4* c3 = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
-                    const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
-                    const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
-                    dot2_mxfp4(c1, s1, c3, s3, xr, cnt, p.H / 32, lane, g, u);
-                }
-#pragma unroll
-                for (int t = 0; t < TG; ++t) {
-                    g[t] = warp_sum(g[t]);
-                    u[t] = warp_sum(u[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < TG; ++t)
-                    if (t < cnt && lane == t)
-                        hdst[(size_t)(pbase + q0 + t) * inter + i] = f32_to_bf16_bits(silu_mul(g[t], u[t]));
+                reset_arrival();
             }
         }
         release();
         return true;
+    }
+
+    // Down projection: output row r (relative to the CTA's first row h0)
+    // belongs to warp (r - h0) % NCW for every slot, so each y element is
+    // accumulated by one lane in slot order.
+    template <int NT>
+    __device__ __forceinline__ void down_group(const uint8_t* st, const Chunk& ch, int j, int qa, int qb, bool shared,
+                                               size_t sofs, float (&acc)[NT]) const {
+        const LayerParams& p = x.p;
+        const int inter = shared ? p.Is : p.I;
+        const size_t hb = (size_t)ch.np * inter * 2;
+        const uint4* h0 = reinterpret_cast<const uint4*>(st + (size_t)qa * inter * 2);
+        const uint4* h1 = reinterpret_cast<const uint4*>(st + (size_t)qb * inter * 2);
+        if (WFMT == 0 || shared) {
+            const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * inter * 2);
+            dot_bf16<NT>(row, h0, h1, inter / 8, lane, acc);
+        } else {
+            const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * (p.I / 2));
+            const uint8_t* sc = st + hb + (size_t)ch.n * (p.I / 2) + sofs + (size_t)j * (p.I / 32);
+            dot_mxfp4<NT>(row, sc, h0, h1, p.I / 32, lane, acc);
+        }
+    }
+
+    __device__ __forceinline__ void combine(const Chunk& ch, int pbase, bool shared, int qq, int r, int h0,
+                                            float v) const {
+        const int pp = ch.p0 + qq;
+        const int tok = shared ? pp : plan->pair_tok[pbase + pp];
+        const float wt = shared ? 1.0f : plan->pair_w[pbase + pp];
+        float* ya = yacc + (size_t)tok * x.p.rpc + (r - h0);
+        *ya = fmaf(wt, v, *ya);
     }
 
     __device__ bool down(const Chunk& ch, int h0) {
@@ -556,46 +721,30 @@ struct Consumer {
         const LayerParams& p = x.p;
         const uint8_t* st = stage_ptr();
         const bool shared = ch.slot < 0;
-        const int inter = shared ? p.Is : p.I;
-        const size_t hb = (size_t)ch.np * inter * 2;
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
         size_t sofs = 0;
         if (WFMT == 1 && !shared) {
             size_t s0 = ((size_t)slot_expert(x, ch.slot) * p.H + ch.r0) * (p.I / 32);
             sofs = s0 - (s0 & ~(size_t)15);
         }
-        for (int j = 0; j < ch.n; ++j) {
-            const int r = ch.r0 + j;
-            if ((r - h0) % NCW != warp) continue;
-            for (int q0 = 0; q0 < ch.np; q0 += TG) {
-                int cnt = min(TG, ch.np - q0);
-                const uint4* hr[TG];
-#pragma unroll
-                for (int t = 0; t < TG; ++t)
-                    hr[t] = reinterpret_cast<const uint4*>(st + (size_t)min(q0 + t, ch.np - 1) * inter * 2);
-                float acc[TG] = {0.f, 0.f, 0.f, 0.f};
-                if (WFMT == 0 || shared) {
-                    const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * inter * 2);
-                    dot_bf16(row, hr, cnt, inter / 8, lane, acc);
-                } else {
-                    const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * (p.I / 2));
-                    const uint8_t* sc = st + hb + (size_t)ch.n * (p.I / 2) + sofs + (size_t)j * (p.I / 32);
-                    dot_mxfp4(row, sc, hr, cnt, p.I / 32, lane, acc);
-                }
-#pragma unroll
-                for (int t = 0; t < TG; ++t) acc[t] = warp_sum(acc[t]);
+        for (int r = ch.r0 + ((warp - (ch.r0 - h0)) % NCW + NCW) % NCW; r < ch.r0 + ch.n; r += NCW) {
+            const int j = r - ch.r0;
+            int q0 = 0;
+            for (; q0 + 2 <= ch.np; q0 += 2) {
+                float acc[2];
+                down_group<2>(st, ch, j, q0, q0 + 1, shared, sofs, acc);
+                acc[0] = warp_sum(acc[0]);
+                acc[1] = warp_sum(acc[1]);
                 if (lane == 0) {
-#pragma unroll
-                    for (int t = 0; t < TG; ++t) {
-                        if (t < cnt) {
-                            int pp = ch.p0 + q0 + t;
-                            int tok = shared ? pp : plan->pair_tok[pbase + pp];
-                            float wt = shared ? 1.0f : plan->pair_w[pbase + pp];
-                            float* ya = yacc + (size_t)tok * p.rpc + (r - h0);
-                            *ya = fmaf(wt, acc[t], *ya);
-                        }
-                    }
+                    combine(ch, pbase, shared, q0, r, h0, acc[0]);
+                    combine(ch, pbase, shared, q0 + 1, r, h0, acc[1]);
                 }
+            }
+            if (q0 < ch.np) {
+                float acc[1];
+                down_group<1>(st, ch, j, q0, q0, shared, sofs, acc);
+                acc[0] = warp_sum(acc[0]);
+                if (lane == 0) combine(ch, pbase, shared, q0, r, h0, acc[0]);
             }
         }
         release();
@@ -605,85 +754,103 @@ struct Consumer {
 
 // ------------------------------------------------------------ routing + plan
 
-// Softmax, top-k (descending logit, ties to the lower index) and
-// renormalisation for the tokens of this warp; writes plan->sel_e / sel_w.
-static __device__ void topk_tokens(const LayerParams& p, Plan* plan, int warp, int lane) {
-    for (int t = warp; t < p.M; t += NCW) {
-        const float* lrow = p.logits + (size_t)t * p.E;
-        float v[32];
-        uint32_t taken = 0;
-        float mx = -INFINITY;
+// Order-preserving map of an fp32 value to a u32 key (larger value ->
+// larger key), and back; hardware warp reductions on u32 then rank logits.
+__device__ __forceinline__ uint32_t f32_key(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_f32(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Orders (key desc, index asc) in a register list of N entries with a
+// bitonic network (N a power of two; all indices compile-time).
+template <int N>
+__device__ __forceinline__ void sort_desc(uint32_t (&key)[N], uint32_t (&idx)[N]) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            int e = lane + 32 * j;
-            if (e < p.E) {
-                v[j] = __ldcg(lrow + e);
-                mx = fmaxf(mx, v[j]);
-            } else {
-                v[j] = -INFINITY;
-                taken |= 1u << j;
-            }
-        }
+    for (int k2 = 2; k2 <= N; k2 <<= 1) {
 #pragma unroll
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        int sel[kMaxK];
-        float selv[kMaxK];
+        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
 #pragma unroll
-        for (int jj = 0; jj < kMaxK; ++jj) {
-            sel[jj] = 0;
-            selv[jj] = 0.f;
-            if (jj < p.k) {
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (!((taken >> j) & 1u) && (v[j] > bv || be == 0x7fffffff)) {
-                        bv = v[j];
-                        be = lane + 32 * j;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o; o >>= 1) {
-                    float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                sel[jj] = be;
-                selv[jj] = bv;
-            }
-        }
-        float ex[kMaxK], den = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < kMaxK; ++jj) {
-            ex[jj] = 0.f;
-            if (jj < p.k) {
-                ex[jj] = expf(selv[jj] - mx);
-                den += ex[jj];
-            }
-        }
-        if (lane == 0) {
-#pragma unroll
-            for (int jj = 0; jj < kMaxK; ++jj) {
-                if (jj < p.k) {
-                    plan->sel_e[t * p.k + jj] = sel[jj];
-                    plan->sel_w[t * p.k + jj] = ex[jj] / den;
+            for (int i = 0; i < N; ++i) {
+                const int l = i ^ j2;
+                if (l > i) {
+                    // after this step, for a descending block, position i holds the "larger" entry
+                    const bool desc = (i & k2) == 0;
+                    const uint32_t ki = key[i], kl = key[l], ii = idx[i], il = idx[l];
+                    const bool l_first = kl > ki || (kl == ki && il < ii);
+                    const bool sw = l_first == desc;  // branch-free exchange
+                    key[i] = sw ? kl : ki;
+                    key[l] = sw ? ki : kl;
+                    idx[i] = sw ? il : ii;
+                    idx[l] = sw ? ii : il;
                 }
             }
         }
     }
 }
 
+// Softmax, top-k (descending logit, ties to the lower expert index) and
+// renormalisation for the tokens of this warp; writes plan->sel_e / sel_w.
+// Each lane loads the logits e = lane + 32 j (EPL of them), sorts them once,
+// and each of the k rounds takes the warp maximum with one hardware
+// reduction, the lowest expert index among the lanes holding it with a
+// second, and pops the winner from the winning lane's list. The full softmax
+// denominator cancels in the renormalisation, so
+// w_j = exp(l_j - max) / sum over the selected of exp(l - max).
+template <int EPL>
+__device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int E, const int k, int lane,
+                                          int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
+    uint32_t key[EPL], idx[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        idx[j] = (uint32_t)e;
+        key[j] = e < E ? f32_key(__ldcg(lrow + e)) : 0u;
+    }
+    sort_desc<EPL>(key, idx);
+    float mx = 0.f, mine_val = 0.f;
+    for (int jj = 0; jj < k; ++jj) {
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t we = __reduce_min_sync(0xffffffffu, key[0] == wk ? idx[0] : 0xffffffffu);
+        const float wv = key_f32(wk);
+        if (jj == 0) mx = wv;
+        if (lane == jj) mine_val = wv;
+        if (lane == 0) sel_e[jj] = (int32_t)we;
+        if ((we & 31u) == (uint32_t)lane) {
+#pragma unroll
+            for (int j = 0; j + 1 < EPL; ++j) {
+                key[j] = key[j + 1];
+                idx[j] = idx[j + 1];
+            }
+            key[EPL - 1] = 0u;
+        }
+    }
+    const float ex = lane < k ? expf(mine_val - mx) : 0.f;
+    float den = ex;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    if (lane < k) sel_w[lane] = ex / den;
+}
+
+static __device__ __forceinline__ void topk_tokens(const float* __restrict__ logits, const int M, const int E,
+                                                   const int k, Plan* plan, int warp, int lane, int nwarps) {
+    for (int t = warp; t < M; t += nwarps) {
+        const float* lrow = logits + (size_t)t * E;
+        if (E <= 512)
+            topk_warp<16>(lrow, E, k, lane, plan->sel_e + t * k, plan->sel_w + t * k);
+        else
+            topk_warp<32>(lrow, E, k, lane, plan->sel_e + t * k, plan->sel_w + t * k);
+    }
+}
 
 // Groups the M*k (token, expert) entries by expert with one pairwise pass per
 // entry: rank = (#entries with a smaller expert id) + (#earlier entries with
 // the same id). Nothing here scales with E. Entries whose expert id lies
 // outside [0, E) (possible only when the routing is given) are dropped and
 // reported.
-static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, bool report) {
+static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, int nct, bool report) {
     const int N = p.M * p.k;
     const int BIG = 0x7fffffff;
     int e = BIG, less = 0;
@@ -705,7 +872,7 @@ static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, boo
         plan->rank[tid] = less + before;
         plan->first[tid] = (valid && before == 0) ? 1 : 0;
     }
-    named_bar_sync(1, NCT);
+    named_bar_sync(1, nct);
     if (tid < N && valid) {
         int r = plan->rank[tid];
         plan->pair_tok[r] = (int16_t)(tid / p.k);
@@ -729,12 +896,14 @@ static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, boo
         plan->npairs = np;
         plan->slot_p0[u] = (int16_t)np;
     }
-    named_bar_sync(1, NCT);
+    named_bar_sync(1, nct);
 }
 
 // ------------------------------------------------------------ the kernel
 template <int WFMT>
-__global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
+__global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
+    constexpr int NCW = consumer_warps(WFMT);
+    constexpr int NCT = NCW * 32;
     extern __shared__ __align__(1024) uint8_t smem[];
     // Early trigger: the next launch on the stream may start its prologue
     // (weight prefetch) as soon as SMs free up; it still waits for this grid
@@ -754,9 +923,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
         }
         mbar_init(plan_bar, 1);
         plan->abort = 0;
+        for (int i = 0; i < kMaxStages; ++i) plan->arrive[i] = 0;
         fence_mbar_init();
     }
     __syncthreads();
+    if (tid == 0) trace_mark(p, 0);
 
     const Ctx cx{p, (int)blockIdx.x, plan};
     const Ring ring0{smem_u32(smem), bars, p.ns, 0};
@@ -765,6 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
     if (warp == NCW) {
         // ---------------- producer (one elected lane)
         if (lane == 0) {
+            trace_mark(p, 8);
             Producer<WFMT> pr{cx, ring0, plan, policy_evict_first(), policy_evict_last(), false, 0, {}, 0};
             bool ok = true;
             auto issue = [&](const Chunk& c) {
@@ -773,14 +945,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             // producer-independent tiles: router rows, shared expert gate/up
             if (has_route) for_router_chunks(cx, issue);
             if (has_ffn) for_shared_gateup_chunks<WFMT>(cx, issue);
+            trace_mark(p, 9);
             pdl_wait();
             if (ok && has_ffn) {
                 ok = mbar_wait(plan_bar, 0, p, plan);
+                trace_mark(p, 10);
                 if (ok) for_routed_gateup_chunks<WFMT>(cx, issue);
+                trace_mark(p, 11);
                 if (ok) for_down_chunks<WFMT>(cx, issue);
+                trace_mark(p, 12);
                 if (ok) ok = pr.poll_b2(true);
+                trace_mark(p, 13);
             }
             if (!ok || aborted(plan)) pr.drain();
+            trace_mark(p, 14);
         }
     } else {
         // ---------------- consumers
@@ -799,28 +977,26 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 }
         }
         named_bar_sync(1, NCT);
+        if (tid == 0) trace_mark(p, 1);
         bool ok = true;
         if (has_route) {
             for_router_chunks(cx, [&](const Chunk& c) {
                 if (ok) ok = cs.router(c);
             });
             named_bar_sync(1, NCT);  // this CTA's logits are stored
+            if (tid == 0) trace_mark(p, 2);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar1, 1u);
             }
         }
         cs.q = 0;
-        // the shared expert needs no routing: compute it while barrier 1 fills
-        if (has_ffn)
-            for_shared_gateup_chunks<WFMT>(cx, [&](const Chunk& c) {
-                if (ok) ok = cs.gateup(c);
-            });
         if (has_route) {
             if (tid == 0 && !aborted(plan))
                 grid_wait(p.ctrl + kCtlBar1, (unsigned)p.G + (p.force_timeout ? 1u : 0u), p, plan);
             named_bar_sync(1, NCT);
-            if (!aborted(plan)) topk_tokens(p, plan, warp, lane);
+            if (tid == 0) trace_mark(p, 4);
+            if (!aborted(plan)) topk_tokens(p.logits, p.M, p.E, p.k, plan, warp, lane, NCW);
             named_bar_sync(1, NCT);
             if (blockIdx.x == 0 && !aborted(plan)) {
                 for (int i = tid; i < p.M * p.k; i += NCT) {
@@ -830,12 +1006,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
             }
         }
         if (has_ffn) {
-            build_plan(p, plan, tid, blockIdx.x == 0);
-            if (tid == 0) mbar_arrive(plan_bar);
+            build_plan(p, plan, tid, NCT, blockIdx.x == 0);
+            if (tid == 0) {
+                mbar_arrive(plan_bar);
+                trace_mark(p, 5);
+            }
+            // the shared expert's tiles were fetched before routing finished;
+            // computing them now overlaps the first routed tiles' latency
+            for_shared_gateup_chunks<WFMT>(cx, [&](const Chunk& c) {
+                if (ok && !aborted(plan)) ok = cs.gateup(c);
+            });
             for_routed_gateup_chunks<WFMT>(cx, [&](const Chunk& c) {
                 if (ok && !aborted(plan)) ok = cs.gateup(c);
             });
             named_bar_sync(1, NCT);  // this CTA's activations are stored
+            if (tid == 0) trace_mark(p, 6);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar2, 1u);
@@ -846,6 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_layer_kernel(const __grid_con
                 if (ok && !aborted(plan)) ok = cs.down(c, h0);
             });
             named_bar_sync(1, NCT);
+            if (tid == 0) trace_mark(p, 7);
             if (!aborted(plan)) {
                 const int nr = h1 - h0;
                 for (int i = tid; i < p.M * nr; i += NCT) {

@@ -5,15 +5,19 @@
 
 namespace moe {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kConsumerThreads = kConsumerWarps * 32;
+// Consumer warps per CTA for each routed-weight format; one producer warp
+// comes on top. The totals (16 and 8 warps) spread evenly over the SM's four
+// schedulers, which keeps the per-thread register budget at 128 and 255.
+constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 15 : 7; }
+constexpr int block_threads(int wfmt) { return (consumer_warps(wfmt) + 1) * 32; }
 constexpr uint32_t kStageBytes = 32768;               // one ring stage
 constexpr int kMaxStages = 6;
 constexpr int kMaxM = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
+constexpr int kSplitUnits = 16;  // (row, K-slice) units of a split-K chunk
+constexpr int kSplitPairs = 16;  // tokens per unit held as partial sums
 
 // workspace control block (uint32 words; counters 128 bytes apart)
 constexpr int kCtlStatus = 0;
@@ -52,6 +56,7 @@ struct LayerParams {
     int rpc;               // rows of y owned per CTA, upper bound (ceil(H/G))
     int force_timeout;
     unsigned long long timeout_ns;
+    unsigned long long* trace;  // optional [G][16] phase timestamps (ns), may be null
     uint32_t off_bar, off_plan, off_x, off_yacc, smem_bytes;
 };
 
@@ -69,6 +74,10 @@ struct Plan {
     int32_t npairs;
     int32_t abort;
     int32_t pad;
+    // Split-K partial sums of the chunk in each ring stage (router rows or
+    // gate/up row pairs): [unit][pair][gate, up], units = rows x K-slices.
+    float part[kMaxStages][kSplitUnits * kSplitPairs * 2];
+    int32_t arrive[kMaxStages];  // warps done with the stage's chunk
 };
 
 
