@@ -42,9 +42,6 @@
 namespace moe {
 
 constexpr uint32_t SB = kStageBytes;
-// Split a chunk's rows along K over all consumer warps (off: measured slower
-// than giving each row to one warp, see the split_ns comment).
-constexpr bool kSplitK = false;
 
 // A unit of the ring: the tiles one stage holds.
 struct Chunk {
@@ -54,64 +51,15 @@ struct Chunk {
     int p0, np; // down: pair range within the slot
 };
 
-struct Ctx {
-    const LayerParams& p;
-    int c;  // CTA index
-    const Plan* plan;
-};
-
-__device__ __forceinline__ int slot_expert(const Ctx& x, int s) { return x.plan->slot_e[s]; }
-
-__device__ __forceinline__ int slot_npairs(const Ctx& x, int s) {
-    return s < 0 ? x.p.M : x.plan->slot_p0[s + 1] - x.plan->slot_p0[s];
-}
-
 // ------------------------------------------------------------ chunk lists
-// The producer and the consumers enumerate identical chunk sequences.
-
-template <class F>
-__device__ __forceinline__ void for_router_chunks(const Ctx& x, F&& f) {
-    const LayerParams& p = x.p;
-    int e0 = (int)((long long)x.c * p.E / p.G), e1 = (int)((long long)(x.c + 1) * p.E / p.G);
-    int cap = (int)(SB / (uint32_t)(p.H * 2));
-    for (int r = e0; r < e1; r += cap) f(Chunk{0, -1, r, min(cap, e1 - r), 0, 0});
-}
-
+// The producer and the consumers step identical ChunkGen instances, so both
+// sides agree on every chunk. Phases: 0 router rows, 1 shared-expert gate/up
+// rows, 2 routed gate/up rows (needs the plan), 3 down rows (needs the plan).
+// next() returns false at the end of each phase; begin(ph) starts a phase.
 template <int WFMT>
 __device__ __forceinline__ int gateup_cap(const LayerParams& p, bool routed) {
     uint32_t pair = (WFMT == 1 && routed) ? (uint32_t)(2 * (p.H / 2 + p.H / 32)) : (uint32_t)(4 * p.H);
     return (int)(SB / pair);
-}
-
-template <int WFMT, class F>
-__device__ __forceinline__ void for_shared_gateup_chunks(const Ctx& x, F&& f) {
-    const LayerParams& p = x.p;
-    if (p.Is <= 0) return;
-    int i0 = (int)((long long)x.c * p.Is / p.G), i1 = (int)((long long)(x.c + 1) * p.Is / p.G);
-    int cap = gateup_cap<WFMT>(p, false);
-    for (int r = i0; r < i1; r += cap) f(Chunk{1, -1, r, min(cap, i1 - r), 0, 0});
-}
-
-template <int WFMT, class F>
-__device__ __forceinline__ void for_routed_gateup_chunks(const Ctx& x, F&& f) {
-    const LayerParams& p = x.p;
-    const uint32_t I = (uint32_t)p.I;
-    const uint32_t R = (uint32_t)x.plan->nslot * I;  // <= 256 * 4096
-    const uint32_t G = (uint32_t)p.G, c = (uint32_t)x.c;
-    uint32_t r = (uint32_t)(((uint64_t)c * R) / G), r1 = (uint32_t)(((uint64_t)(c + 1) * R) / G);
-    const uint32_t cap = (uint32_t)gateup_cap<WFMT>(p, true);
-    if (r >= r1) return;
-    uint32_t s = r / I, i0 = r - s * I;
-    while (r < r1) {
-        uint32_t n = min(cap, min(r1 - r, I - i0));
-        f(Chunk{1, (int)s, (int)i0, (int)n, 0, 0});
-        r += n;
-        i0 += n;
-        if (i0 == I) {
-            i0 = 0;
-            ++s;
-        }
-    }
 }
 
 template <int WFMT>
@@ -120,25 +68,88 @@ __device__ __forceinline__ uint32_t down_rowbytes(const LayerParams& p, int slot
     return WFMT == 1 ? (uint32_t)(p.I / 2 + p.I / 32) : (uint32_t)p.I * 2;
 }
 
-template <int WFMT, class F>
-__device__ __forceinline__ void for_down_chunks(const Ctx& x, F&& f) {
-    const LayerParams& p = x.p;
-    int h0 = (int)((long long)x.c * p.H / p.G), h1 = (int)((long long)(x.c + 1) * p.H / p.G);
-    if (h1 <= h0) return;
-    for (int s = (p.Is > 0 ? -1 : 0); s < x.plan->nslot; ++s) {
-        int inter = s < 0 ? p.Is : p.I;
-        uint32_t hrow = (uint32_t)inter * 2;
-        uint32_t rowb = down_rowbytes<WFMT>(p, s);
-        uint32_t reserve = (WFMT == 1 && s >= 0) ? 32u : 0u;
-        int npairs = slot_npairs(x, s);
-        int pg = max(1, min(npairs, (int)((SB / 2) / hrow)));
-        for (int q0 = 0; q0 < npairs; q0 += pg) {
-            int np = min(pg, npairs - q0);
-            int cap = (int)((SB - (uint32_t)np * hrow - reserve) / rowb);
-            for (int r = h0; r < h1; r += cap) f(Chunk{2, s, r, min(cap, h1 - r), q0, np});
+template <int WFMT>
+struct ChunkGen {
+    int phase;
+    int a, b, cap;                 // phases 0, 1: row cursor, end, rows per chunk
+    uint32_t r, r1, slot, i0, I;   // phase 2: flattened routed rows
+    int ds, nslot, q0, npairs, pg, h, h0, h1;  // phase 3
+
+    __device__ __forceinline__ void begin(int ph, const LayerParams& p, const Plan* plan, int c) {
+        phase = ph;
+        const uint32_t G = (uint32_t)p.G, cc = (uint32_t)c;
+        if (ph == 0) {
+            a = (int)(cc * (uint32_t)p.E / G);
+            b = (int)((cc + 1) * (uint32_t)p.E / G);
+            cap = (int)(SB / (uint32_t)(p.H * 2));
+        } else if (ph == 1) {
+            a = (int)(cc * (uint32_t)p.Is / G);
+            b = (int)((cc + 1) * (uint32_t)p.Is / G);
+            cap = gateup_cap<WFMT>(p, false);
+        } else if (ph == 2) {
+            I = (uint32_t)p.I;
+            const uint32_t R = (uint32_t)plan->nslot * I;  // <= 256 * 4096
+            r = (uint32_t)(((uint64_t)cc * R) / G);
+            r1 = (uint32_t)(((uint64_t)(cc + 1) * R) / G);
+            slot = r / I;
+            i0 = r - slot * I;
+            cap = gateup_cap<WFMT>(p, true);
+        } else {
+            nslot = plan->nslot;
+            h0 = (int)(cc * (uint32_t)p.H / G);
+            h1 = (int)((cc + 1) * (uint32_t)p.H / G);
+            ds = (p.Is > 0 ? -1 : 0) - 1;
+            npairs = 0;
+            q0 = 0;
+            pg = 1;
+            h = h1;  // forces the next slot on the first call
         }
     }
-}
+
+    __device__ __forceinline__ bool next(const LayerParams& p, const Plan* plan, Chunk& ch) {
+        if (phase <= 1) {
+            if (a >= b) return false;
+            const int n = min(cap, b - a);
+            ch = Chunk{phase == 0 ? 0 : 1, -1, a, n, 0, 0};
+            a += n;
+            return true;
+        }
+        if (phase == 2) {
+            if (r >= r1) return false;
+            const uint32_t n = min((uint32_t)cap, min(r1 - r, I - i0));
+            ch = Chunk{1, (int)slot, (int)i0, (int)n, 0, 0};
+            r += n;
+            i0 += n;
+            if (i0 == I) {
+                i0 = 0;
+                ++slot;
+            }
+            return true;
+        }
+        // phase 3: slots (shared first), pair groups, row chunks
+        if (h1 <= h0) return false;
+        if (h >= h1) {
+            q0 += pg;
+            if (q0 >= npairs) {
+                if (++ds >= nslot) return false;
+                npairs = ds < 0 ? p.M : plan->slot_p0[ds + 1] - plan->slot_p0[ds];
+                const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * 2;
+                pg = max(1, min(npairs, (int)((SB / 2) / hrow)));
+                q0 = 0;
+            }
+            h = h0;
+        }
+        const int inter = ds < 0 ? p.Is : p.I;
+        const uint32_t hrow = (uint32_t)inter * 2;
+        const uint32_t reserve = (WFMT == 1 && ds >= 0) ? 32u : 0u;
+        const int np = min(pg, npairs - q0);
+        const int rcap = (int)((SB - (uint32_t)np * hrow - reserve) / down_rowbytes<WFMT>(p, ds));
+        const int n = min(rcap, h1 - h);
+        ch = Chunk{2, ds, h, n, q0, np};
+        h += n;
+        return true;
+    }
+};
 
 // Optional phase trace: slot i of this CTA's 16-entry record gets the global
 // timer (ns). Slots 0-7 are written by consumer thread 0, 8-15 by the
@@ -193,88 +204,103 @@ __device__ __forceinline__ bool grid_wait(const unsigned* ctr, unsigned target, 
     return true;
 }
 
-// ------------------------------------------------------------ producer
+// ------------------------------------------------------------ ring
+// Stage cursor of the shared-memory ring, advanced chunk by chunk (no
+// divisions). Chunk n lives in stage n % ns and is the (n / ns)-th use of it;
+// ph is the parity of that use.
 struct Ring {
     uint32_t base;  // shared address of stage 0
-    uint32_t bars;  // full[ns] then empty[ns]
-    int ns;
-    uint32_t n;     // chunks issued / consumed so far
-    __device__ __forceinline__ uint32_t stage(uint32_t i) const { return base + (i % ns) * SB; }
-    __device__ __forceinline__ uint32_t full(uint32_t i) const { return bars + (i % ns) * 8; }
-    __device__ __forceinline__ uint32_t empty(uint32_t i) const { return bars + (ns + i % ns) * 8; }
-    __device__ __forceinline__ uint32_t parity(uint32_t i) const { return (i / ns) & 1u; }
+    uint32_t bars;  // full[ns], then empty[ns]
+    uint32_t ns;
+    uint32_t n, s, ph;
+    __device__ __forceinline__ uint32_t stage() const { return base + s * SB; }
+    __device__ __forceinline__ uint32_t full() const { return bars + s * 8; }
+    __device__ __forceinline__ uint32_t empty() const { return bars + (ns + s) * 8; }
+    __device__ __forceinline__ void advance() {
+        ++n;
+        if (++s == ns) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
 };
 
-struct Pending {
-    uint32_t dst, bytes, bar;
-    const void* src;
-};
-
+// ------------------------------------------------------------ producer
+// One elected lane. Weight tiles of a chunk are issued as soon as its stage
+// is free; the activation tiles of a down chunk are produced by all CTAs and
+// may only be fetched after grid barrier 2, so until then they wait in a
+// short list in shared memory.
 template <int WFMT>
 struct Producer {
-    const Ctx& x;
-    Ring ring;
+    const LayerParams& p;
     Plan* plan;
-    uint64_t pol_w;    // weights: evict first
-    uint64_t pol_h;    // activations: keep
+    Ring ring;
+    uint64_t pol_w;  // weights: evict first
+    uint64_t pol_h;  // activations: keep
     bool b2_done;
-    int npend;
-    Pending pend[kMaxStages];
     uint32_t complete_upto;  // chunks whose copies were all issued
 
-    __device__ bool poll_b2(bool block) {
+    __device__ __forceinline__ void flush_pending() {
+        for (int i = 0; i < plan->npend; ++i)
+            bulk_g2s(plan->pend_dst[i], plan->pend_src[i], plan->pend_bytes[i], plan->pend_bar[i], pol_h);
+        plan->npend = 0;
+        complete_upto = ring.n;
+    }
+
+    __device__ __forceinline__ bool poll_b2(bool block) {
         if (b2_done) return true;
-        const unsigned* ctr = x.p.ctrl + kCtlBar2;
-        bool ok = block ? grid_wait(ctr, (unsigned)x.p.G, x.p, plan) : (ld_acquire_gpu(ctr) >= (unsigned)x.p.G);
+        const unsigned* ctr = p.ctrl + kCtlBar2;
+        const bool ok = block ? grid_wait(ctr, (unsigned)p.G, p, plan) : (ld_acquire_gpu(ctr) >= (unsigned)p.G);
         if (!ok) return false;
         b2_done = true;
         fence_proxy_async_global();
-        for (int i = 0; i < npend; ++i) bulk_g2s(pend[i].dst, pend[i].src, pend[i].bytes, pend[i].bar, pol_h);
-        npend = 0;
-        complete_upto = ring.n;
+        flush_pending();
         return true;
     }
 
-    // Waits for the stage of chunk ring.n to be free. In phase 2 it keeps
-    // polling barrier 2 meanwhile, so that deferred activation copies go out
-    // as soon as they may.
-    __device__ bool acquire(bool phase2) {
-        uint32_t i = ring.n;
-        if (i < (uint32_t)ring.ns) return true;
-        uint32_t bar = ring.empty(i), par = ring.parity(i) ^ 1u;
+    // Waits until the stage of the next chunk is free. In phase 2 it polls
+    // without suspending, so that barrier 2 is seen as soon as it completes.
+    __device__ __forceinline__ bool acquire(bool down) {
+        if (ring.n < ring.ns) return true;
+        const uint32_t bar = ring.empty(), par = ring.ph ^ 1u;
         if (mbar_test_wait(bar, par)) return true;
-        uint64_t t0 = global_timer_ns();
-        while (true) {
-            // suspend for at most ~0.25 us at a time, so that barrier 2 is
-            // polled promptly during phase 2
-            if (mbar_try_wait_hint(bar, par, phase2 ? 256u : 100000u)) return true;
-            if (phase2) poll_b2(false);
-            if (aborted(plan)) return false;
-            if (global_timer_ns() - t0 > x.p.timeout_ns) {
-                set_abort(x.p, plan, -101);
-                return false;
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+            if (down) {
+                if (mbar_test_wait(bar, par)) return true;
+                poll_b2(false);
+                __nanosleep(32);
+            } else if (mbar_try_wait(bar, par)) {
+                return true;
+            }
+            if ((spin & 15u) == 0) {
+                if (aborted(plan)) return false;
+                if (global_timer_ns() - t0 > p.timeout_ns) {
+                    set_abort(p, plan, -101 /* MOE_ETIMEOUT */);
+                    return false;
+                }
             }
         }
     }
 
-    __device__ bool issue(const Chunk& ch) {
-        const LayerParams& p = x.p;
+    __device__ __forceinline__ bool issue(const Chunk& ch) {
         if (aborted(plan)) return false;
         if (!acquire(ch.kind == 2)) return false;
-        uint32_t dst = ring.stage(ring.n), bar = ring.full(ring.n);
+        const uint32_t dst = ring.stage(), bar = ring.full();
+        bool deferred = false;
         if (ch.kind == 0) {
-            uint32_t b = (uint32_t)ch.n * p.H * 2;
+            const uint32_t b = (uint32_t)ch.n * p.H * 2;
             mbar_arrive_expect_tx(bar, b);
             bulk_g2s(dst, p.Wg + (size_t)ch.r0 * p.H, b, bar, pol_w);
         } else if (ch.kind == 1) {
             if (ch.slot < 0 || WFMT == 0) {
-                uint32_t b = (uint32_t)ch.n * p.H * 2;
+                const uint32_t b = (uint32_t)ch.n * p.H * 2;
                 const uint8_t *a, *c;
                 if (ch.slot < 0) {
                     a = reinterpret_cast<const uint8_t*>(p.ws1 + (size_t)ch.r0 * p.H);
                     c = reinterpret_cast<const uint8_t*>(p.ws3 + (size_t)ch.r0 * p.H);
                 } else {
-                    size_t off = ((size_t)slot_expert(x, ch.slot) * p.I + ch.r0) * p.H * 2;
+                    const size_t off = ((size_t)plan->slot_e[ch.slot] * p.I + ch.r0) * p.H * 2;
                     a = p.w1 + off;
                     c = p.w3 + off;
                 }
@@ -282,8 +308,8 @@ struct Producer {
                 bulk_g2s(dst, a, b, bar, pol_w);
                 bulk_g2s(dst + b, c, b, bar, pol_w);
             } else {
-                uint32_t bc = (uint32_t)ch.n * (p.H / 2), bs = (uint32_t)ch.n * (p.H / 32);
-                size_t row = (size_t)slot_expert(x, ch.slot) * p.I + ch.r0;
+                const uint32_t bc = (uint32_t)ch.n * (p.H / 2), bs = (uint32_t)ch.n * (p.H / 32);
+                const size_t row = (size_t)plan->slot_e[ch.slot] * p.I + ch.r0;
                 mbar_arrive_expect_tx(bar, 2 * bc + 2 * bs);
                 bulk_g2s(dst, p.w1 + row * (p.H / 2), bc, bar, pol_w);
                 bulk_g2s(dst + bc, p.w3 + row * (p.H / 2), bc, bar, pol_w);
@@ -291,29 +317,27 @@ struct Producer {
                 bulk_g2s(dst + 2 * bc + bs, p.s3 + row * (p.H / 32), bs, bar, pol_w);
             }
         } else {
-            int inter = ch.slot < 0 ? p.Is : p.I;
-            uint32_t hb = (uint32_t)ch.np * inter * 2;
+            const int inter = ch.slot < 0 ? p.Is : p.I;
+            const uint32_t hb = (uint32_t)ch.np * inter * 2;
             const void* hsrc;
-            uint32_t wbytes;
             if (ch.slot < 0) {
                 hsrc = p.hs + (size_t)ch.p0 * p.Is;
-                wbytes = (uint32_t)ch.n * p.Is * 2;
-                mbar_arrive_expect_tx(bar, hb + wbytes);
-                bulk_g2s(dst + hb, p.ws2 + (size_t)ch.r0 * p.Is, wbytes, bar, pol_w);
+                const uint32_t wb = (uint32_t)ch.n * p.Is * 2;
+                mbar_arrive_expect_tx(bar, hb + wb);
+                bulk_g2s(dst + hb, p.ws2 + (size_t)ch.r0 * p.Is, wb, bar, pol_w);
             } else {
-                hsrc = p.hr + (size_t)(x.plan->slot_p0[ch.slot] + ch.p0) * p.I;
-                size_t row = (size_t)slot_expert(x, ch.slot) * p.H + ch.r0;
+                hsrc = p.hr + (size_t)(plan->slot_p0[ch.slot] + ch.p0) * p.I;
+                const size_t row = (size_t)plan->slot_e[ch.slot] * p.H + ch.r0;
                 if (WFMT == 0) {
-                    wbytes = (uint32_t)ch.n * p.I * 2;
-                    mbar_arrive_expect_tx(bar, hb + wbytes);
-                    bulk_g2s(dst + hb, p.w2 + row * p.I * 2, wbytes, bar, pol_w);
+                    const uint32_t wb = (uint32_t)ch.n * p.I * 2;
+                    mbar_arrive_expect_tx(bar, hb + wb);
+                    bulk_g2s(dst + hb, p.w2 + row * p.I * 2, wb, bar, pol_w);
                 } else {
-                    uint32_t bc = (uint32_t)ch.n * (p.I / 2);
-                    size_t s0 = row * (p.I / 32), s1 = s0 + (size_t)ch.n * (p.I / 32);
-                    size_t w0 = s0 & ~(size_t)15, w1 = (s1 + 15) & ~(size_t)15;
-                    uint32_t bs = (uint32_t)(w1 - w0);
-                    wbytes = bc + bs;
-                    mbar_arrive_expect_tx(bar, hb + wbytes);
+                    const uint32_t bc = (uint32_t)ch.n * (p.I / 2);
+                    const size_t s0 = row * (p.I / 32), s1 = s0 + (size_t)ch.n * (p.I / 32);
+                    const size_t w0 = s0 & ~(size_t)15, w1 = (s1 + 15) & ~(size_t)15;
+                    const uint32_t bs = (uint32_t)(w1 - w0);
+                    mbar_arrive_expect_tx(bar, hb + bc + bs);
                     bulk_g2s(dst + hb, p.w2 + row * (p.I / 2), bc, bar, pol_w);
                     bulk_g2s(dst + hb + bc, p.s2 + w0, bs, bar, pol_w);
                 }
@@ -321,29 +345,32 @@ struct Producer {
             if (b2_done) {
                 bulk_g2s(dst, hsrc, hb, bar, pol_h);
             } else {
-                pend[npend++] = Pending{dst, hb, bar, hsrc};
-                ring.n++;
-                return true;
+                const int k = plan->npend++;
+                plan->pend_dst[k] = dst;
+                plan->pend_src[k] = hsrc;
+                plan->pend_bytes[k] = hb;
+                plan->pend_bar[k] = bar;
+                deferred = true;
             }
         }
-        ring.n++;
-        if (npend == 0) complete_upto = ring.n;
+        ring.advance();
+        if (!deferred && plan->npend == 0) complete_upto = ring.n;
         return true;
     }
 
     // After an abort: wait (bounded) for every copy already issued, so that
     // no bulk copy is still writing this CTA's shared memory at exit.
+    // Deferred activation copies are issued regardless (their source is valid
+    // workspace memory), so that every stage's barrier can complete.
     __device__ void drain() {
-        // Deferred activation copies are issued regardless (their source is
-        // valid workspace memory), so that every stage's barrier can complete.
-        for (int i = 0; i < npend; ++i) bulk_g2s(pend[i].dst, pend[i].src, pend[i].bytes, pend[i].bar, pol_h);
-        npend = 0;
-        complete_upto = ring.n;
-        uint32_t lo = complete_upto > (uint32_t)ring.ns ? complete_upto - ring.ns : 0;
-        for (uint32_t i = lo; i < complete_upto; ++i) {
-            uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(ring.full(i), ring.parity(i))) {
-                if (global_timer_ns() - t0 > x.p.timeout_ns) break;
+        flush_pending();
+        const uint32_t n = complete_upto;
+        const uint32_t lo = n > ring.ns ? n - ring.ns : 0;
+        for (uint32_t i = lo; i < n; ++i) {
+            const uint32_t bar = ring.bars + (i % ring.ns) * 8, par = (i / ring.ns) & 1u;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(bar, par)) {
+                if (global_timer_ns() - t0 > p.timeout_ns) break;
             }
         }
     }
@@ -488,243 +515,128 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 template <int WFMT>
 struct Consumer {
     static constexpr int NCW = consumer_warps(WFMT);
-    const Ctx& x;
-    Ring ring;
+    const LayerParams& p;
     Plan* plan;
+    Ring ring;
     const uint16_t* xs;  // tokens in shared memory [M][H]
     float* yacc;         // [M][rpc]
-    int warp, lane, tid;
+    int warp, lane;
     int q;               // running row counter (row ownership)
+    int h0;              // first output row of this CTA
 
-    __device__ __forceinline__ bool wait_full() {
-        return mbar_wait(ring.full(ring.n), ring.parity(ring.n), x.p, plan);
-    }
+    __device__ __forceinline__ bool wait_full() { return mbar_wait(ring.full(), ring.ph, p, plan); }
     __device__ __forceinline__ void release() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(ring.empty(ring.n));
-        ring.n++;
+        if (lane == 0) mbar_arrive(ring.empty());
+        ring.advance();
     }
     __device__ __forceinline__ const uint8_t* stage_ptr() const {
-        return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(ring.stage(ring.n)));
+        return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(ring.stage()));
     }
     __device__ __forceinline__ const uint4* xrow(int tok) const {
-        return reinterpret_cast<const uint4*>(xs + (size_t)tok * x.p.H);
+        return reinterpret_cast<const uint4*>(xs + (size_t)tok * p.H);
     }
 
-    __device__ __forceinline__ float* part_buf() const { return plan->part[ring.n % ring.ns]; }
-
-    // Split-K layout of a chunk of n rows whose reduction dimension spans ncol
-    // columns of 32 lanes: NS slices per row so that the n * NS units keep
-    // every consumer warp busy. NS = 1 means no split.
-    __device__ __forceinline__ int split_ns(int n, int ncol, int npairs) const {
-        if (!kSplitK || n >= NCW || npairs > kSplitPairs || ncol < 2) return 1;
-        return max(1, min(NCW / n, min(ncol, kSplitUnits / n)));
-    }
-
-    // Called by every consumer warp once per split chunk, after its partial
-    // sums are stored: returns true in the last warp to arrive, which then
-    // sees every warp's partials.
-    __device__ __forceinline__ bool last_to_arrive() const {
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            old = atomicAdd(&plan->arrive[ring.n % ring.ns], 1);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != NCW - 1) return false;
-        __threadfence_block();
-        return true;
-    }
-    __device__ __forceinline__ void reset_arrival() const {
-        __syncwarp();
-        if (lane == 0) plan->arrive[ring.n % ring.ns] = 0;
-    }
-
-    __device__ bool router(const Chunk& ch) {
-        if (!wait_full()) return false;
-        const LayerParams& p = x.p;
-        const uint8_t* st = stage_ptr();
-        const int ncol = p.H / 256;
-        const int NS = split_ns(ch.n, ncol, p.M);
-        if (NS == 1) {
-            for (int j = 0; j < ch.n; ++j, ++q) {
-                if (q % NCW != warp) continue;
-                const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
-                for (int t = 0; t < p.M; ++t) {
-                    float acc[1];
-                    dot_bf16<1>(row, xrow(t), xrow(t), p.H / 8, lane, acc);
-                    acc[0] = warp_sum(acc[0]);
-                    if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
-                }
-            }
-        } else {
-            q += ch.n;
-            const int cs = (ncol + NS - 1) / NS;
-            float* part = part_buf();
-            if (warp < ch.n * NS) {
-                const int j = warp / NS, sl = warp - j * NS;
-                const int c0 = sl * cs, c1 = min(ncol, c0 + cs);
-                const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
-                for (int t = 0; t < p.M; ++t) {
-                    float acc[1];
-                    dot_bf16<1>(row, xrow(t), xrow(t), 32 * c1, lane + 32 * c0, acc);
-                    acc[0] = warp_sum(acc[0]);
-                    if (lane == 0) part[(warp * kSplitPairs + t) * 2] = acc[0];
-                }
-            }
-            if (last_to_arrive()) {
-                for (int it = lane; it < ch.n * p.M; it += 32) {
-                    const int j = it / p.M, t = it - j * p.M;
-                    float v = 0.f;
-                    for (int s2 = 0; s2 < NS; ++s2) v += part[((j * NS + s2) * kSplitPairs + t) * 2];
-                    p.logits[(size_t)t * p.E + ch.r0 + j] = v;
-                }
-                reset_arrival();
+    // Router rows: logits[t][e] = Wg[e] . x_t, one warp per row.
+    __device__ __forceinline__ void router(const Chunk& ch, const uint8_t* st) {
+        const int nvec = p.H / 8;
+        for (int j = 0; j < ch.n; ++j, ++q) {
+            if (q % NCW != warp) continue;
+            const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
+            for (int t = 0; t < p.M; ++t) {
+                float acc[1];
+                dot_bf16<1>(row, xrow(t), xrow(t), nvec, lane, acc);
+                acc[0] = warp_sum(acc[0]);
+                if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
             }
         }
-        release();
-        return true;
     }
 
-    // Gate/up dot products of row pair j over lane columns [c0, c1) for two
-    // (or one) tokens.
     template <int NT>
     __device__ __forceinline__ void gateup_group(const uint8_t* st, const Chunk& ch, int j, int t0tok, int t1tok,
-                                                 bool shared, int c0, int c1, float (&g)[NT], float (&u)[NT]) const {
-        const LayerParams& p = x.p;
+                                                 bool shared, float (&g)[NT], float (&u)[NT]) const {
         if (WFMT == 0 || shared) {
             const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
-            dot2_bf16<NT>(r1, r3, xrow(t0tok), xrow(t1tok), min(32 * c1, p.H / 8), lane + 32 * c0, g, u);
+            dot2_bf16<NT>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
         } else {
             const size_t cb = (size_t)p.H / 2, sbytes = (size_t)p.H / 32;
-            const uint4* c1p = reinterpret_cast<const uint4*>(st + j * cb);
-            const uint4* c3p = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
+            const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
+            const uint4* c3 = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
             const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
             const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
-            dot2_mxfp4<NT>(c1p, s1, c3p, s3, xrow(t0tok), xrow(t1tok), min(32 * c1, p.H / 32), lane + 32 * c0, g, u);
+            dot2_mxfp4<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
         }
     }
 
-    // All tokens of the slot against row pair j over lane columns [c0, c1);
-    // out(pair, g, u) receives the warp-reduced sums (valid in lane 0).
-    template <class Out>
-    __device__ __forceinline__ void gateup_row(const uint8_t* st, const Chunk& ch, int j, bool shared, int npairs,
-                                               int pbase, int c0, int c1, Out&& out) const {
-        int q0 = 0;
-        for (; q0 + 2 <= npairs; q0 += 2) {
-            const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
-            const int tb = shared ? q0 + 1 : plan->pair_tok[pbase + q0 + 1];
-            float g[2], u[2];
-            gateup_group<2>(st, ch, j, ta, tb, shared, c0, c1, g, u);
-            g[0] = warp_sum(g[0]);
-            u[0] = warp_sum(u[0]);
-            g[1] = warp_sum(g[1]);
-            u[1] = warp_sum(u[1]);
-            out(q0, g[0], u[0]);
-            out(q0 + 1, g[1], u[1]);
-        }
-        if (q0 < npairs) {
-            const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
-            float g[1], u[1];
-            gateup_group<1>(st, ch, j, ta, ta, shared, c0, c1, g, u);
-            g[0] = warp_sum(g[0]);
-            u[0] = warp_sum(u[0]);
-            out(q0, g[0], u[0]);
-        }
-    }
-
-    __device__ bool gateup(const Chunk& ch) {
-        if (!wait_full()) return false;
-        const LayerParams& p = x.p;
-        const uint8_t* st = stage_ptr();
+    // Gate/up rows: one warp per row pair, all tokens of the slot; stores
+    // h = silu(g) * u in bf16.
+    __device__ __forceinline__ void gateup(const Chunk& ch, const uint8_t* st) {
         const bool shared = ch.slot < 0;
         const int inter = shared ? p.Is : p.I;
-        const int npairs = slot_npairs(x, ch.slot);
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
+        const int npairs = shared ? p.M : plan->slot_p0[ch.slot + 1] - pbase;
         uint16_t* hdst = (shared ? p.hs : p.hr) + (size_t)pbase * inter + ch.r0;
-        const int ncol = (WFMT == 0 || shared) ? p.H / 256 : (p.H / 32 + 31) / 32;
-        const int NS = split_ns(ch.n, ncol, npairs);
-        if (NS == 1) {
-            for (int j = 0; j < ch.n; ++j, ++q) {
-                if (q % NCW != warp) continue;
-                gateup_row(st, ch, j, shared, npairs, pbase, 0, ncol, [&](int pr, float g, float u) {
-                    if (lane == 0) hdst[(size_t)pr * inter + j] = f32_to_bf16_bits(silu_mul(g, u));
-                });
+        for (int j = 0; j < ch.n; ++j, ++q) {
+            if (q % NCW != warp) continue;
+            int q0 = 0;
+            for (; q0 + 2 <= npairs; q0 += 2) {
+                const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
+                const int tb = shared ? q0 + 1 : plan->pair_tok[pbase + q0 + 1];
+                float g[2], u[2];
+                gateup_group<2>(st, ch, j, ta, tb, shared, g, u);
+                g[0] = warp_sum(g[0]);
+                u[0] = warp_sum(u[0]);
+                g[1] = warp_sum(g[1]);
+                u[1] = warp_sum(u[1]);
+                if (lane < 2)
+                    hdst[(size_t)(q0 + lane) * inter + j] =
+                        f32_to_bf16_bits(silu_mul(lane ? g[1] : g[0], lane ? u[1] : u[0]));
             }
-        } else {
-            q += ch.n;
-            const int cs = (ncol + NS - 1) / NS;
-            float* part = part_buf();
-            if (warp < ch.n * NS) {
-                const int j = warp / NS, sl = warp - j * NS;
-                const int c0 = sl * cs, c1 = min(ncol, c0 + cs);
-                float* mine = part + warp * kSplitPairs * 2;
-                gateup_row(st, ch, j, shared, npairs, pbase, c0, c1, [&](int pr, float g, float u) {
-                    if (lane == 0) {
-                        mine[pr * 2] = g;
-                        mine[pr * 2 + 1] = u;
-                    }
-                });
-            }
-            if (last_to_arrive()) {
-                for (int it = lane; it < ch.n * npairs; it += 32) {
-                    const int j = it / npairs, pr = it - j * npairs;
-                    float g = 0.f, u = 0.f;
-                    for (int s2 = 0; s2 < NS; ++s2) {
-                        const float* src = part + ((j * NS + s2) * kSplitPairs + pr) * 2;
-                        g += src[0];
-                        u += src[1];
-                    }
-                    hdst[(size_t)pr * inter + j] = f32_to_bf16_bits(silu_mul(g, u));
-                }
-                reset_arrival();
+            if (q0 < npairs) {
+                const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
+                float g[1], u[1];
+                gateup_group<1>(st, ch, j, ta, ta, shared, g, u);
+                g[0] = warp_sum(g[0]);
+                u[0] = warp_sum(u[0]);
+                if (lane == 0) hdst[(size_t)q0 * inter + j] = f32_to_bf16_bits(silu_mul(g[0], u[0]));
             }
         }
-        release();
-        return true;
     }
 
-    // Down projection: output row r (relative to the CTA's first row h0)
-    // belongs to warp (r - h0) % NCW for every slot, so each y element is
-    // accumulated by one lane in slot order.
     template <int NT>
     __device__ __forceinline__ void down_group(const uint8_t* st, const Chunk& ch, int j, int qa, int qb, bool shared,
                                                size_t sofs, float (&acc)[NT]) const {
-        const LayerParams& p = x.p;
         const int inter = shared ? p.Is : p.I;
         const size_t hb = (size_t)ch.np * inter * 2;
-        const uint4* h0 = reinterpret_cast<const uint4*>(st + (size_t)qa * inter * 2);
-        const uint4* h1 = reinterpret_cast<const uint4*>(st + (size_t)qb * inter * 2);
+        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)qa * inter * 2);
+        const uint4* hb_ = reinterpret_cast<const uint4*>(st + (size_t)qb * inter * 2);
         if (WFMT == 0 || shared) {
             const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * inter * 2);
-            dot_bf16<NT>(row, h0, h1, inter / 8, lane, acc);
+            dot_bf16<NT>(row, ha, hb_, inter / 8, lane, acc);
         } else {
             const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * (p.I / 2));
             const uint8_t* sc = st + hb + (size_t)ch.n * (p.I / 2) + sofs + (size_t)j * (p.I / 32);
-            dot_mxfp4<NT>(row, sc, h0, h1, p.I / 32, lane, acc);
+            dot_mxfp4<NT>(row, sc, ha, hb_, p.I / 32, lane, acc);
         }
     }
 
-    __device__ __forceinline__ void combine(const Chunk& ch, int pbase, bool shared, int qq, int r, int h0,
-                                            float v) const {
+    __device__ __forceinline__ void combine(const Chunk& ch, int pbase, bool shared, int qq, int r, float v) const {
         const int pp = ch.p0 + qq;
         const int tok = shared ? pp : plan->pair_tok[pbase + pp];
         const float wt = shared ? 1.0f : plan->pair_w[pbase + pp];
-        float* ya = yacc + (size_t)tok * x.p.rpc + (r - h0);
+        float* ya = yacc + (size_t)tok * p.rpc + (r - h0);
         *ya = fmaf(wt, v, *ya);
     }
 
-    __device__ bool down(const Chunk& ch, int h0) {
-        if (!wait_full()) return false;
-        const LayerParams& p = x.p;
-        const uint8_t* st = stage_ptr();
+    // Down projection: output row r belongs to warp (r - h0) % NCW for every
+    // slot, so each y element is accumulated by one lane in slot order.
+    __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
         const bool shared = ch.slot < 0;
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
         size_t sofs = 0;
         if (WFMT == 1 && !shared) {
-            size_t s0 = ((size_t)slot_expert(x, ch.slot) * p.H + ch.r0) * (p.I / 32);
+            const size_t s0 = ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * (p.I / 32);
             sofs = s0 - (s0 & ~(size_t)15);
         }
         for (int r = ch.r0 + ((warp - (ch.r0 - h0)) % NCW + NCW) % NCW; r < ch.r0 + ch.n; r += NCW) {
@@ -736,17 +648,29 @@ struct Consumer {
                 acc[0] = warp_sum(acc[0]);
                 acc[1] = warp_sum(acc[1]);
                 if (lane == 0) {
-                    combine(ch, pbase, shared, q0, r, h0, acc[0]);
-                    combine(ch, pbase, shared, q0 + 1, r, h0, acc[1]);
+                    combine(ch, pbase, shared, q0, r, acc[0]);
+                    combine(ch, pbase, shared, q0 + 1, r, acc[1]);
                 }
             }
             if (q0 < ch.np) {
                 float acc[1];
                 down_group<1>(st, ch, j, q0, q0, shared, sofs, acc);
                 acc[0] = warp_sum(acc[0]);
-                if (lane == 0) combine(ch, pbase, shared, q0, r, h0, acc[0]);
+                if (lane == 0) combine(ch, pbase, shared, q0, r, acc[0]);
             }
         }
+    }
+
+    // Waits for the next chunk, computes this warp's share, frees the stage.
+    __device__ __forceinline__ bool consume(const Chunk& ch) {
+        if (!wait_full()) return false;
+        const uint8_t* st = stage_ptr();
+        if (ch.kind == 0)
+            router(ch, st);
+        else if (ch.kind == 1)
+            gateup(ch, st);
+        else
+            down(ch, st);
         release();
         return true;
     }
@@ -911,6 +835,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
     pdl_launch_dependents();
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = (int)blockIdx.x;
     Plan* plan = reinterpret_cast<Plan*>(smem + p.off_plan);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + p.off_x);
     float* yacc = reinterpret_cast<float*>(smem + p.off_yacc);
@@ -923,36 +848,38 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         }
         mbar_init(plan_bar, 1);
         plan->abort = 0;
-        for (int i = 0; i < kMaxStages; ++i) plan->arrive[i] = 0;
+        plan->npend = 0;
         fence_mbar_init();
     }
     __syncthreads();
     if (tid == 0) trace_mark(p, 0);
 
-    const Ctx cx{p, (int)blockIdx.x, plan};
-    const Ring ring0{smem_u32(smem), bars, p.ns, 0};
+    const Ring ring0{smem_u32(smem), bars, (uint32_t)p.ns, 0u, 0u, 0u};
     const bool has_route = (p.mode & kModeRoute) != 0, has_ffn = (p.mode & kModeFfn) != 0;
+    ChunkGen<WFMT> gen;
+    Chunk ch;
 
     if (warp == NCW) {
         // ---------------- producer (one elected lane)
         if (lane == 0) {
             trace_mark(p, 8);
-            Producer<WFMT> pr{cx, ring0, plan, policy_evict_first(), policy_evict_last(), false, 0, {}, 0};
+            Producer<WFMT> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u};
             bool ok = true;
-            auto issue = [&](const Chunk& c) {
-                if (ok) ok = pr.issue(c);
-            };
-            // producer-independent tiles: router rows, shared expert gate/up
-            if (has_route) for_router_chunks(cx, issue);
-            if (has_ffn) for_shared_gateup_chunks<WFMT>(cx, issue);
+            // producer-independent tiles: router rows, shared-expert gate/up rows
+            if (has_route)
+                for (gen.begin(0, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
+            if (has_ffn)
+                for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
             trace_mark(p, 9);
             pdl_wait();
             if (ok && has_ffn) {
                 ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
-                if (ok) for_routed_gateup_chunks<WFMT>(cx, issue);
+                if (ok)
+                    for (gen.begin(2, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
                 trace_mark(p, 11);
-                if (ok) for_down_chunks<WFMT>(cx, issue);
+                if (ok)
+                    for (gen.begin(3, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
                 trace_mark(p, 12);
                 if (ok) ok = pr.poll_b2(true);
                 trace_mark(p, 13);
@@ -962,7 +889,9 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         }
     } else {
         // ---------------- consumers
-        Consumer<WFMT> cs{cx, ring0, plan, xs, yacc, warp, lane, tid, 0};
+        const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
+        const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
+        Consumer<WFMT> cs{p, plan, ring0, xs, yacc, warp, lane, 0, h0};
         pdl_wait();
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
@@ -980,25 +909,19 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         if (tid == 0) trace_mark(p, 1);
         bool ok = true;
         if (has_route) {
-            for_router_chunks(cx, [&](const Chunk& c) {
-                if (ok) ok = cs.router(c);
-            });
+            for (gen.begin(0, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
             named_bar_sync(1, NCT);  // this CTA's logits are stored
             if (tid == 0) trace_mark(p, 2);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar1, 1u);
-            }
-        }
-        cs.q = 0;
-        if (has_route) {
-            if (tid == 0 && !aborted(plan))
                 grid_wait(p.ctrl + kCtlBar1, (unsigned)p.G + (p.force_timeout ? 1u : 0u), p, plan);
+            }
             named_bar_sync(1, NCT);
             if (tid == 0) trace_mark(p, 4);
             if (!aborted(plan)) topk_tokens(p.logits, p.M, p.E, p.k, plan, warp, lane, NCW);
             named_bar_sync(1, NCT);
-            if (blockIdx.x == 0 && !aborted(plan)) {
+            if (cta == 0 && !aborted(plan)) {
                 for (int i = tid; i < p.M * p.k; i += NCT) {
                     if (p.idx_out) p.idx_out[i] = plan->sel_e[i];
                     if (p.w_out) p.w_out[i] = plan->sel_w[i];
@@ -1006,36 +929,29 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             }
         }
         if (has_ffn) {
-            build_plan(p, plan, tid, NCT, blockIdx.x == 0);
+            build_plan(p, plan, tid, NCT, cta == 0);
             if (tid == 0) {
                 mbar_arrive(plan_bar);
                 trace_mark(p, 5);
             }
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
-            for_shared_gateup_chunks<WFMT>(cx, [&](const Chunk& c) {
-                if (ok && !aborted(plan)) ok = cs.gateup(c);
-            });
-            for_routed_gateup_chunks<WFMT>(cx, [&](const Chunk& c) {
-                if (ok && !aborted(plan)) ok = cs.gateup(c);
-            });
+            cs.q = 0;
+            for (gen.begin(1, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            for (gen.begin(2, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar2, 1u);
             }
-            const int h0 = (int)((long long)blockIdx.x * p.H / p.G);
-            const int h1 = (int)((long long)(blockIdx.x + 1) * p.H / p.G);
-            for_down_chunks<WFMT>(cx, [&](const Chunk& c) {
-                if (ok && !aborted(plan)) ok = cs.down(c, h0);
-            });
+            for (gen.begin(3, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
             named_bar_sync(1, NCT);
             if (tid == 0) trace_mark(p, 7);
             if (!aborted(plan)) {
                 const int nr = h1 - h0;
                 for (int i = tid; i < p.M * nr; i += NCT) {
-                    int t = i / nr, r = i - t * nr;
+                    const int t = i / nr, r = i - t * nr;
                     p.y[(size_t)t * p.H + h0 + r] = f32_to_bf16_bits(yacc[(size_t)t * p.rpc + r]);
                 }
             }
@@ -1045,7 +961,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
     if (tid == 0 && !aborted(plan)) {
         // Last CTA out re-arms the barrier counters for the next call.
         __threadfence();
-        unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
+        const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
         if (old == (unsigned)p.G - 1u) {
             atomicExch(p.ctrl + kCtlBar1, 0u);
             atomicExch(p.ctrl + kCtlBar2, 0u);

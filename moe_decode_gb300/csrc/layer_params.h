@@ -6,9 +6,9 @@
 namespace moe {
 
 // Consumer warps per CTA for each routed-weight format; one producer warp
-// comes on top. The totals (16 and 8 warps) spread evenly over the SM's four
-// schedulers, which keeps the per-thread register budget at 128 and 255.
-constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 15 : 7; }
+// comes on top. The totals (12 and 8 warps) spread evenly over the SM's four
+// schedulers, which keeps the per-thread register budget at 168 and 255.
+constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 11 : 7; }
 constexpr int block_threads(int wfmt) { return (consumer_warps(wfmt) + 1) * 32; }
 constexpr uint32_t kStageBytes = 32768;               // one ring stage
 constexpr int kMaxStages = 6;
@@ -16,8 +16,6 @@ constexpr int kMaxM = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
-constexpr int kSplitUnits = 16;  // (row, K-slice) units of a split-K chunk
-constexpr int kSplitPairs = 16;  // tokens per unit held as partial sums
 
 // workspace control block (uint32 words; counters 128 bytes apart)
 constexpr int kCtlStatus = 0;
@@ -74,10 +72,11 @@ struct Plan {
     int32_t npairs;
     int32_t abort;
     int32_t pad;
-    // Split-K partial sums of the chunk in each ring stage (router rows or
-    // gate/up row pairs): [unit][pair][gate, up], units = rows x K-slices.
-    float part[kMaxStages][kSplitUnits * kSplitPairs * 2];
-    int32_t arrive[kMaxStages];  // warps done with the stage's chunk
+    // Activation copies of down chunks issued before grid barrier 2
+    // (producer only): destination, barrier, bytes, source.
+    uint32_t pend_dst[kMaxStages], pend_bar[kMaxStages], pend_bytes[kMaxStages];
+    const void* pend_src[kMaxStages];
+    int32_t npend;
 };
 
 
