@@ -118,7 +118,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
 
     const size_t other_plan = align_up(sizeof(moe::Plan), 128);
     const size_t x_bytes = align_up((size_t)M * p.H * 2, 128);
-    const size_t y_bytes = align_up((size_t)M * p.rpc * 4, 128);
+    // down-projection results per (pair, output row): [M + M*k][rpc]
+    const size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
     const size_t bar_bytes = 128;
     size_t fixed = other_plan + x_bytes + y_bytes + bar_bytes;
     if ((size_t)dev.smem_optin <= fixed) return MOE_ESHAPE;

@@ -73,7 +73,7 @@ struct ChunkGen {
     int phase;
     int a, b, cap;                 // phases 0, 1: row cursor, end, rows per chunk
     uint32_t r, r1, slot, i0, I;   // phase 2: flattened routed rows
-    int ds, nslot, q0, npairs, pg, h, h0, h1;  // phase 3
+    int ds, nslot, q0, npairs, pg, np, rcap, h, h0, h1;  // phase 3
 
     __device__ __forceinline__ void begin(int ph, const LayerParams& p, const Plan* plan, int c) {
         phase = ph;
@@ -102,6 +102,8 @@ struct ChunkGen {
             npairs = 0;
             q0 = 0;
             pg = 1;
+            np = 0;
+            rcap = 1;
             h = h1;  // forces the next slot on the first call
         }
     }
@@ -137,13 +139,13 @@ struct ChunkGen {
                 pg = max(1, min(npairs, (int)((SB / 2) / hrow)));
                 q0 = 0;
             }
+            // chunk geometry of this (slot, pair group), computed once
+            const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * 2;
+            const uint32_t reserve = (WFMT == 1 && ds >= 0) ? 32u : 0u;
+            np = min(pg, npairs - q0);
+            rcap = (int)((SB - (uint32_t)np * hrow - reserve) / down_rowbytes<WFMT>(p, ds));
             h = h0;
         }
-        const int inter = ds < 0 ? p.Is : p.I;
-        const uint32_t hrow = (uint32_t)inter * 2;
-        const uint32_t reserve = (WFMT == 1 && ds >= 0) ? 32u : 0u;
-        const int np = min(pg, npairs - q0);
-        const int rcap = (int)((SB - (uint32_t)np * hrow - reserve) / down_rowbytes<WFMT>(p, ds));
         const int n = min(rcap, h1 - h);
         ch = Chunk{2, ds, h, n, q0, np};
         h += n;
@@ -446,6 +448,38 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
     sum4<NT>(pu, u);
 }
 
+// Four rows (row0 + j * rstride, j < 4) against NT vectors at once: the four
+// rows' loads and FMA chains are independent, so one warp keeps several
+// rows in flight instead of finishing them one after another.
+template <int NT>
+__device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rstride, const uint4* __restrict__ h0,
+                                          const uint4* __restrict__ h1, int nvec, int lane, float (&acc)[4][NT]) {
+    float pa[4][NT][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) pa[j][t][0] = pa[j][t][1] = 0.f;
+#pragma unroll 2
+    for (int v = lane; v < nvec; v += 32) {
+        float fh[NT][8];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) unpack8((t == 0 ? h0 : h1)[v], fh[t]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float fw[8];
+            unpack8(row0[j * rstride + v], fw);
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pa[j][t][e & 1] = fmaf(fw[e], fh[t][e], pa[j][t][e & 1]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[j][t] = pa[j][t][0] + pa[j][t][1];
+}
+
 // One 32-element MXFP4 block (16 code bytes) against 32 bf16 values of each
 // token; returns the unscaled block sums.
 template <int NT>
@@ -519,10 +553,11 @@ struct Consumer {
     Plan* plan;
     Ring ring;
     const uint16_t* xs;  // tokens in shared memory [M][H]
-    float* yacc;         // [M][rpc]
+    float* ypair;        // down results per (pair, output row) [M + M*k][rpc]
     int warp, lane;
     int q;               // running row counter (row ownership)
     int h0;              // first output row of this CTA
+    int c3;              // down chunks seen so far
 
     __device__ __forceinline__ bool wait_full() { return mbar_wait(ring.full(), ring.ph, p, plan); }
     __device__ __forceinline__ void release() {
@@ -545,7 +580,8 @@ struct Consumer {
             const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             for (int t = 0; t < p.M; ++t) {
                 float acc[1];
-                dot_bf16<1>(row, xrow(t), xrow(t), nvec, lane, acc);
+                const uint4* xt = xrow(t);
+                dot_bf16<1>(row, xt, xt, nvec, lane, acc);
                 acc[0] = warp_sum(acc[0]);
                 if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
             }
@@ -621,42 +657,106 @@ struct Consumer {
         }
     }
 
-    __device__ __forceinline__ void combine(const Chunk& ch, int pbase, bool shared, int qq, int r, float v) const {
-        const int pp = ch.p0 + qq;
-        const int tok = shared ? pp : plan->pair_tok[pbase + pp];
-        const float wt = shared ? 1.0f : plan->pair_w[pbase + pp];
-        float* ya = yacc + (size_t)tok * p.rpc + (r - h0);
-        *ya = fmaf(wt, v, *ya);
-    }
-
-    // Down projection: output row r belongs to warp (r - h0) % NCW for every
-    // slot, so each y element is accumulated by one lane in slot order.
+    // Down projection. A down chunk (one slot, a pair group, a block of
+    // output rows) is split into DG parts of consecutive rows, and part j of
+    // the c-th down chunk goes to warp (c * DG + j) % NCW, so the chunks that
+    // are resident together are worked on by different warps at the same
+    // time. Each (pair, row) result is written exactly once, unweighted, into
+    // ypair; the weighted combine runs after the last chunk, in pair order.
     __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
+        const int DG = (NCW + p.ns - 1) / p.ns;
+        const int c = c3++;
         const bool shared = ch.slot < 0;
-        const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
+        const int gbase = (shared ? 0 : p.M + plan->slot_p0[ch.slot]) + ch.p0;  // pair index of q0 = 0
         size_t sofs = 0;
         if (WFMT == 1 && !shared) {
             const size_t s0 = ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * (p.I / 32);
             sofs = s0 - (s0 & ~(size_t)15);
         }
-        for (int r = ch.r0 + ((warp - (ch.r0 - h0)) % NCW + NCW) % NCW; r < ch.r0 + ch.n; r += NCW) {
-            const int j = r - ch.r0;
-            int q0 = 0;
-            for (; q0 + 2 <= ch.np; q0 += 2) {
-                float acc[2];
-                down_group<2>(st, ch, j, q0, q0 + 1, shared, sofs, acc);
-                acc[0] = warp_sum(acc[0]);
-                acc[1] = warp_sum(acc[1]);
-                if (lane == 0) {
-                    combine(ch, pbase, shared, q0, r, acc[0]);
-                    combine(ch, pbase, shared, q0 + 1, r, acc[1]);
+        const int inter = shared ? p.Is : p.I;
+        for (int part = 0; part < DG; ++part) {
+            if ((c * DG + part) % NCW != warp) continue;
+            const int ra = ch.r0 + part * ch.n / DG, rb = ch.r0 + (part + 1) * ch.n / DG;
+            if (WFMT == 0 || shared) {
+                const size_t hb = (size_t)ch.np * inter * 2;
+                const int rstride = inter / 8;  // uint4 per row
+                for (int r = ra; r < rb; r += 4) {
+                    const int nrow = min(4, rb - r);
+                    const uint4* row0 = reinterpret_cast<const uint4*>(st + hb + (size_t)(r - ch.r0) * inter * 2);
+                    float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
+                    int q0 = 0;
+                    for (; q0 + 2 <= ch.np; q0 += 2) {
+                        float acc[4][2];
+                        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
+                        if (nrow == 4) {
+                            dot4_bf16<2>(row0, rstride, ha, ha + rstride, rstride, lane, acc);
+                        } else {  // a partial block: the valid rows one at a time
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] = acc[jj][1] = 0.f;
+                            for (int jj = 0; jj < nrow; ++jj) {
+                                float a1[2];
+                                dot_bf16<2>(row0 + jj * rstride, ha, ha + rstride, rstride, lane, a1);
+                                acc[jj][0] = a1[0];
+                                acc[jj][1] = a1[1];
+                            }
+                        }
+#pragma unroll
+                        for (int o = 16; o; o >>= 1)
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
+                                acc[jj][1] += __shfl_xor_sync(0xffffffffu, acc[jj][1], o);
+                            }
+                        if (lane == 0)
+                            for (int jj = 0; jj < nrow; ++jj) {
+                                out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
+                                out[(size_t)(q0 + 1) * p.rpc + jj] = acc[jj][1];
+                            }
+                    }
+                    if (q0 < ch.np) {
+                        float acc[4][1];
+                        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
+                        if (nrow == 4) {
+                            dot4_bf16<1>(row0, rstride, ha, ha, rstride, lane, acc);
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] = 0.f;
+                            for (int jj = 0; jj < nrow; ++jj) {
+                                float a1[1];
+                                dot_bf16<1>(row0 + jj * rstride, ha, ha, rstride, lane, a1);
+                                acc[jj][0] = a1[0];
+                            }
+                        }
+#pragma unroll
+                        for (int o = 16; o; o >>= 1)
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
+                        if (lane == 0)
+                            for (int jj = 0; jj < nrow; ++jj) out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
+                    }
                 }
+                continue;
             }
-            if (q0 < ch.np) {
-                float acc[1];
-                down_group<1>(st, ch, j, q0, q0, shared, sofs, acc);
-                acc[0] = warp_sum(acc[0]);
-                if (lane == 0) combine(ch, pbase, shared, q0, r, acc[0]);
+            for (int r = ra; r < rb; ++r) {
+                const int j = r - ch.r0;
+                float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
+                int q0 = 0;
+                for (; q0 + 2 <= ch.np; q0 += 2) {
+                    float acc[2];
+                    down_group<2>(st, ch, j, q0, q0 + 1, shared, sofs, acc);
+                    acc[0] = warp_sum(acc[0]);
+                    acc[1] = warp_sum(acc[1]);
+                    if (lane == 0) {
+                        out[(size_t)q0 * p.rpc] = acc[0];
+                        out[(size_t)(q0 + 1) * p.rpc] = acc[1];
+                    }
+                }
+                if (q0 < ch.np) {
+                    float acc[1];
+                    down_group<1>(st, ch, j, q0, q0, shared, sofs, acc);
+                    acc[0] = warp_sum(acc[0]);
+                    if (lane == 0) out[(size_t)q0 * p.rpc] = acc[0];
+                }
             }
         }
     }
@@ -688,70 +788,53 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Orders (key desc, index asc) in a register list of N entries with a
-// bitonic network (N a power of two; all indices compile-time).
-template <int N>
-__device__ __forceinline__ void sort_desc(uint32_t (&key)[N], uint32_t (&idx)[N]) {
+// Softmax, top-k (descending logit, ties to the lower expert index) and
+// renormalisation for one token, by one warp. Lane l holds the logits of
+// experts l, l + 32, ... (EPL of them) and keeps its own best entry; each of
+// the k rounds takes the warp maximum with one hardware reduction, the lowest
+// expert index among the lanes holding it with a second, and the winning lane
+// rescans its entries. The code stays small on purpose: it runs once per
+// launch, so its instructions are fetched cold. The full softmax denominator
+// cancels in the renormalisation, so
+// w_j = exp(l_j - max) / sum over the selected of exp(l - max).
+template <int EPL>
+__device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int E, const int k, int lane,
+                                       int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
+    uint32_t key[EPL];
 #pragma unroll
-    for (int k2 = 2; k2 <= N; k2 <<= 1) {
+    for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = e < E ? f32_key(__ldcg(lrow + e)) : 0u;
+    }
+    uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
-        for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+    for (int j = 0; j < EPL; ++j)
+        if (key[j] > bk) {
+            bk = key[j];
+            bi = (uint32_t)(lane + 32 * j);
+        }
+    float mx = 0.f, mine = 0.f;
+    for (int jj = 0; jj < k; ++jj) {
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? bi : 0xffffffffu);
+        const float wv = key_f32(wk);
+        if (jj == 0) mx = wv;
+        if (lane == jj) mine = wv;
+        if (lane == 0) sel_e[jj] = (int32_t)we;
+        if (we == bi) {  // this lane won: drop the entry, find the next best
+            bk = 0u;
+            bi = 0xffffffffu;
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const int l = i ^ j2;
-                if (l > i) {
-                    // after this step, for a descending block, position i holds the "larger" entry
-                    const bool desc = (i & k2) == 0;
-                    const uint32_t ki = key[i], kl = key[l], ii = idx[i], il = idx[l];
-                    const bool l_first = kl > ki || (kl == ki && il < ii);
-                    const bool sw = l_first == desc;  // branch-free exchange
-                    key[i] = sw ? kl : ki;
-                    key[l] = sw ? ki : kl;
-                    idx[i] = sw ? il : ii;
-                    idx[l] = sw ? ii : il;
+            for (int j = 0; j < EPL; ++j) {
+                if ((uint32_t)(lane + 32 * j) == we) key[j] = 0u;
+                if (key[j] > bk) {
+                    bk = key[j];
+                    bi = (uint32_t)(lane + 32 * j);
                 }
             }
         }
     }
-}
-
-// Softmax, top-k (descending logit, ties to the lower expert index) and
-// renormalisation for the tokens of this warp; writes plan->sel_e / sel_w.
-// Each lane loads the logits e = lane + 32 j (EPL of them), sorts them once,
-// and each of the k rounds takes the warp maximum with one hardware
-// reduction, the lowest expert index among the lanes holding it with a
-// second, and pops the winner from the winning lane's list. The full softmax
-// denominator cancels in the renormalisation, so
-// w_j = exp(l_j - max) / sum over the selected of exp(l - max).
-template <int EPL>
-__device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int E, const int k, int lane,
-                                          int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
-    uint32_t key[EPL], idx[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        const int e = lane + 32 * j;
-        idx[j] = (uint32_t)e;
-        key[j] = e < E ? f32_key(__ldcg(lrow + e)) : 0u;
-    }
-    sort_desc<EPL>(key, idx);
-    float mx = 0.f, mine_val = 0.f;
-    for (int jj = 0; jj < k; ++jj) {
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, key[0]);
-        const uint32_t we = __reduce_min_sync(0xffffffffu, key[0] == wk ? idx[0] : 0xffffffffu);
-        const float wv = key_f32(wk);
-        if (jj == 0) mx = wv;
-        if (lane == jj) mine_val = wv;
-        if (lane == 0) sel_e[jj] = (int32_t)we;
-        if ((we & 31u) == (uint32_t)lane) {
-#pragma unroll
-            for (int j = 0; j + 1 < EPL; ++j) {
-                key[j] = key[j + 1];
-                idx[j] = idx[j + 1];
-            }
-            key[EPL - 1] = 0u;
-        }
-    }
-    const float ex = lane < k ? expf(mine_val - mx) : 0.f;
+    const float ex = lane < k ? expf(mine - mx) : 0.f;
     float den = ex;
 #pragma unroll
     for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
@@ -838,7 +921,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
     const int cta = (int)blockIdx.x;
     Plan* plan = reinterpret_cast<Plan*>(smem + p.off_plan);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + p.off_x);
-    float* yacc = reinterpret_cast<float*>(smem + p.off_yacc);
+    float* ypair = reinterpret_cast<float*>(smem + p.off_yacc);
     const uint32_t bars = smem_u32(smem + p.off_bar);
     const uint32_t plan_bar = bars + 2u * p.ns * 8u;
     if (tid == 0) {
@@ -891,14 +974,13 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         // ---------------- consumers
         const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
-        Consumer<WFMT> cs{p, plan, ring0, xs, yacc, warp, lane, 0, h0};
+        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0, 0};
         pdl_wait();
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
             for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
-            for (int i = tid; i < p.M * p.rpc; i += NCT) yacc[i] = 0.f;
             if (!has_route)
                 for (int i = tid; i < p.M * p.k; i += NCT) {
                     plan->sel_e[i] = p.idx_in[i];
@@ -937,22 +1019,28 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
             cs.q = 0;
-            for (gen.begin(1, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
-            for (gen.begin(2, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            for (gen.begin(2, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar2, 1u);
             }
-            for (gen.begin(3, p, plan, cta); ok && !aborted(plan) && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            for (gen.begin(3, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
             named_bar_sync(1, NCT);
             if (tid == 0) trace_mark(p, 7);
             if (!aborted(plan)) {
                 const int nr = h1 - h0;
+                // y[t][r] = shared(t)[r] + sum over routed pairs of token t, in
+                // pair order (experts ascending), of w * down(pair)[r]
+                const int npr = plan->npairs;
                 for (int i = tid; i < p.M * nr; i += NCT) {
                     const int t = i / nr, r = i - t * nr;
-                    p.y[(size_t)t * p.H + h0 + r] = f32_to_bf16_bits(yacc[(size_t)t * p.rpc + r]);
+                    float v = p.Is > 0 ? ypair[(size_t)t * p.rpc + r] : 0.f;
+                    for (int q = 0; q < npr; ++q)
+                        if (plan->pair_tok[q] == t) v = fmaf(plan->pair_w[q], ypair[(size_t)(p.M + q) * p.rpc + r], v);
+                    p.y[(size_t)t * p.H + h0 + r] = f32_to_bf16_bits(v);
                 }
             }
         }
