@@ -69,6 +69,9 @@ extern "C" {
 #define MOE_EALIGN (-5)      /* a pointer is not 16-byte aligned */
 #define MOE_ECUDA (-6)       /* a CUDA runtime call failed */
 #define MOE_ENODEVICE (-7)   /* no usable CUDA device */
+#define MOE_ESCRATCH (-8)    /* moe_decode_layer_static_scratch: the shape
+                                and M need more than
+                                MOE_STATIC_SCRATCH_BYTES of scratch */
 /* written by the device into the workspace status word */
 #define MOE_EDEVICE_BAD_INDEX (-100) /* moe_ffn got an index outside [0, E);
                                         that (token, slot) was skipped */
@@ -79,6 +82,9 @@ extern "C" {
 /* flags of moe_decode_layer */
 #define MOE_F_NO_PDL 1u                /* launch without programmatic
                                           dependent launch */
+#define MOE_F_RESET_SCRATCH 2u          /* moe_decode_layer_static_scratch
+                                          only: zero the static scratch's
+                                          control words before the launch */
 #define MOE_F_DEBUG_FORCE_TIMEOUT 256u /* test hook: the first grid barrier
                                           waits for one CTA more than exists,
                                           so it runs out and reports
@@ -150,6 +156,33 @@ int moe_decode_layer(const void* x, int M, const void* Wg,
                      const moe_weights* weights, const moe_shape* shape,
                      int32_t* idx_out, float* w_out, void* y, void* ws,
                      size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Size of the library's static device scratch (512 KiB: a Ling-3.0-flash
+ * shaped layer needs 255 KiB at M = 16). */
+#define MOE_STATIC_SCRATCH_BYTES 524288u
+
+/* moe_decode_layer without a caller workspace. The papers the library
+ * follows have no counterpart of this entry point: it serves callers that
+ * cannot hand over a workspace. The same kernel, launch configuration and
+ * arithmetic as moe_decode_layer (so the same outputs, bit for bit), but the
+ * workspace is a fixed array of MOE_STATIC_SCRATCH_BYTES in the library's
+ * own device memory (one per device, created when the module loads). The
+ * call allocates and frees nothing; its first call on a device looks the
+ * array up and zeroes its control words on `stream`.
+ *  - Returns MOE_ESCRATCH, before touching the device, when the shape and M
+ *    need more than MOE_STATIC_SCRATCH_BYTES of workspace
+ *    (moe_workspace_bytes > MOE_STATIC_SCRATCH_BYTES).
+ *  - All calls on a device share the one scratch: they must be ordered on
+ *    one stream (or otherwise serialised), also against other threads.
+ *  - flags: MOE_F_NO_PDL, MOE_F_RESET_SCRATCH (needed again only after a
+ *    bounded device wait ran out). The device status word of these calls
+ *    lives in the scratch and is not readable through this ABI.
+ * Other arguments, layouts and errors as moe_decode_layer. */
+int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg,
+                                    const moe_weights* weights,
+                                    const moe_shape* shape, int32_t* idx_out,
+                                    float* w_out, void* y, uint32_t flags,
+                                    void* stream);
 
 /* Synchronises `stream`, then copies the device status word of `ws` to
  * *dev_status (MOE_OK or a device code above). Not for the hot path. */

@@ -19,13 +19,15 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_decode.so")
 
 OK = 0
-EINVAL, ESHAPE, EM, EWORKSPACE, EALIGN, ECUDA, ENODEVICE = -1, -2, -3, -4, -5, -6, -7
+EINVAL, ESHAPE, EM, EWORKSPACE, EALIGN, ECUDA, ENODEVICE, ESCRATCH = -1, -2, -3, -4, -5, -6, -7, -8
 EDEVICE_BAD_INDEX, ETIMEOUT = -100, -101
 F_NO_PDL = 1
+F_RESET_SCRATCH = 2
 F_DEBUG_FORCE_TIMEOUT = 256
 OPT_GRID_CTAS = 1
 OPT_WAIT_TIMEOUT_NS = 2
 OPT_TRACE_BUFFER = 3
+STATIC_SCRATCH_BYTES = 524288
 
 
 class MoeError(RuntimeError):
@@ -57,14 +59,15 @@ def _load():
     lib.moe_route.argtypes = [P, I32, P, sp, P, P, P, SZ, P]
     lib.moe_ffn.argtypes = [P, I32, P, P, wp, sp, P, P, SZ, P]
     lib.moe_decode_layer.argtypes = [P, I32, P, wp, sp, P, P, P, P, SZ, ctypes.c_uint32, P]
+    lib.moe_decode_layer_static_scratch.argtypes = [P, I32, P, wp, sp, P, P, P, ctypes.c_uint32, P]
     lib.moe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_status_str.argtypes = [I32]
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_mxfp4_dequant.argtypes = [P, P, I64, I32, P, P]
     lib.moe_set_option.argtypes = [I32, I64]
     lib.moe_last_launch_count.argtypes = []
-    for f in ("moe_workspace_init", "moe_route", "moe_ffn", "moe_decode_layer", "moe_read_status",
-              "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count"):
+    for f in ("moe_workspace_init", "moe_route", "moe_ffn", "moe_decode_layer", "moe_decode_layer_static_scratch",
+              "moe_read_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count"):
         getattr(lib, f).restype = I32
     return lib
 
@@ -148,6 +151,14 @@ def decode_layer(x, Wg, weights: ExpertWeights, shape: Shape, y, ws, idx_out=Non
     _check(lib.moe_decode_layer(_ptr(x), x.shape[0], _ptr(Wg), ctypes.byref(cw), ctypes.byref(shape),
                                 _ptr(idx_out), _ptr(w_out), _ptr(y), _ptr(ws), ws.numel(), flags,
                                 _stream(stream)), "moe_decode_layer")
+
+
+def decode_layer_static_scratch(x, Wg, weights: ExpertWeights, shape: Shape, y, idx_out=None, w_out=None,
+                                flags: int = 0, stream=None, cweights: Optional[_Weights] = None):
+    cw = cweights if cweights is not None else weights.cstruct()
+    _check(lib.moe_decode_layer_static_scratch(_ptr(x), x.shape[0], _ptr(Wg), ctypes.byref(cw),
+                                               ctypes.byref(shape), _ptr(idx_out), _ptr(w_out), _ptr(y), flags,
+                                               _stream(stream)), "moe_decode_layer_static_scratch")
 
 
 def read_status(ws, stream=None) -> int:

@@ -10,6 +10,10 @@
 #include "launch.h"
 #include "layer_params.h"
 
+// Scratch of moe_decode_layer_static_scratch (a fixed array per device,
+// created with the module).
+static __device__ __align__(256) uint8_t g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 using moe::LayerParams;
@@ -51,6 +55,30 @@ int device_info(DeviceInfo* out) {
         d.coop = coop != 0;
     }
     *out = d;
+    return MOE_OK;
+}
+
+void* g_scratch_ptr[kMaxDevices];
+
+// Device address of this device's static scratch; the first call on a device
+// looks it up and zeroes its control words on `st`.
+int static_scratch(void** out, cudaStream_t st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MOE_ENODEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess ||
+            cudaMemsetAsync(ptr, 0, moe::kCtlBytes, st) != cudaSuccess) {
+            cudaGetLastError();
+            return MOE_ECUDA;
+        }
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
     return MOE_OK;
 }
 
@@ -256,6 +284,37 @@ int moe_decode_layer(const void* x, int M, const void* Wg, const moe_weights* we
     return launch(p, shape->wfmt, static_cast<cudaStream_t>(stream), (flags & MOE_F_NO_PDL) == 0, dev);
 }
 
+int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const moe_weights* weights,
+                                    const moe_shape* shape, int32_t* idx_out, float* w_out, void* y,
+                                    uint32_t flags, void* stream) {
+    g_last_launches = 0;
+    int rc = check_shape(shape, M);
+    if (rc) return rc;
+    if (flags & ~(MOE_F_NO_PDL | MOE_F_RESET_SCRATCH)) return MOE_EINVAL;
+    if (ws_layout(shape, M).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ESCRATCH;
+    if (!x || !Wg || !y || !weights_ok(weights, shape)) return MOE_EINVAL;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(y) || !weights_aligned(weights, shape)) return MOE_EALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = nullptr;
+    rc = static_scratch(&ws, st);
+    if (rc) return rc;
+    if ((flags & MOE_F_RESET_SCRATCH) && cudaMemsetAsync(ws, 0, moe::kCtlBytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
+    LayerParams p = {};
+    DeviceInfo dev;
+    rc = configure(shape, M, moe::kModeLayer, ws, MOE_STATIC_SCRATCH_BYTES, p, dev);
+    if (rc) return rc;
+    p.x = static_cast<const uint16_t*>(x);
+    p.Wg = static_cast<const uint16_t*>(Wg);
+    p.idx_out = idx_out;
+    p.w_out = w_out;
+    p.y = static_cast<uint16_t*>(y);
+    set_weights(p, weights);
+    return launch(p, shape->wfmt, st, (flags & MOE_F_NO_PDL) == 0, dev);
+}
+
 int moe_read_status(const void* ws, void* stream, int32_t* dev_status) {
     if (!ws || !dev_status) return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -280,6 +339,7 @@ const char* moe_status_str(int code) {
         case MOE_EALIGN: return "pointer not 16-byte aligned";
         case MOE_ECUDA: return "CUDA runtime error";
         case MOE_ENODEVICE: return "no usable CUDA device";
+        case MOE_ESCRATCH: return "shape and M need more than the static scratch (MOE_STATIC_SCRATCH_BYTES = 512 KiB)";
         case MOE_EDEVICE_BAD_INDEX: return "device: expert index out of range (entry skipped)";
         case MOE_ETIMEOUT: return "device: bounded wait ran out (outputs incomplete; re-initialise the workspace)";
         default: return "unknown status";
