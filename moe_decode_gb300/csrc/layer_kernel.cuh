@@ -2,9 +2,9 @@
 //
 // One CTA per SM. Each CTA runs one producer warp, whose elected lane streams
 // weight tiles from HBM into a ring of shared-memory stages with bulk (TMA)
-// copies completing on mbarriers, and eight consumer warps that compute from
-// the ring. The layer runs in three phases separated by two bounded grid
-// barriers:
+// copies completing on mbarriers, and consumer warps (consumer_warps(WFMT))
+// that compute from the ring. The layer runs in three phases separated by two
+// bounded grid barriers:
 //
 //   phase 0  router gate matvec: CTA c owns router rows [cE/G, (c+1)E/G);
 //            logits go to the workspace.              -> grid barrier 1
@@ -16,9 +16,10 @@
 //            h = silu(W1 x) * (W3 x) goes to the workspace in bf16.
 //                                                       -> grid barrier 2
 //   phase 2  down projection + weighted combine: CTA c owns output rows
-//            [cH/G, (c+1)H/G) and accumulates, in a fixed order (shared
-//            expert, then routed experts by ascending id, tokens ascending),
-//            w * (W2 h) into fp32, then casts y to bf16 once.
+//            [cH/G, (c+1)H/G); each (token, expert) pair's down result is
+//            kept unweighted in shared memory, then y = shared expert +
+//            sum of w * down over the token's pairs in ascending expert
+//            order, in fp32, cast to bf16 once.
 //
 // Every weight byte of a touched expert is read from HBM exactly once per
 // call, whatever M is. The producer never waits on a grid barrier for weight
