@@ -398,9 +398,26 @@ __device__ __forceinline__ void sum4(const float (&pa)[NT][4], float (&acc)[NT])
     for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0] + pa[t][1]) + (pa[t][2] + pa[t][3]);
 }
 
-// acc[t] = row . x_t (bf16 x bf16, fp32 accumulate) over nvec 16-byte
-// vectors; this lane takes vectors lane, lane + STRIDE, ...
-template <int NT, int STRIDE = 32>
+// Eight activations of one 16-byte vector as fp32: bf16, or (XH) f16.
+template <bool XH>
+__device__ __forceinline__ void unpack8x(const uint4 v, float (&f)[8]) {
+    if (XH) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 a = f16x2_to_f32(w[j]);
+            f[2 * j] = a.x;
+            f[2 * j + 1] = a.y;
+        }
+    } else {
+        unpack8(v, f);
+    }
+}
+
+// acc[t] = row . x_t (bf16 weights, bf16 or (XH) f16 activations, fp32
+// accumulate) over nvec 16-byte vectors; this lane takes vectors lane,
+// lane + STRIDE, ...
+template <int NT, int STRIDE = 32, bool XH = false>
 __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                          const uint4* __restrict__ x1, int nvec, int lane, float (&acc)[NT]) {
     float pa[NT][4];
@@ -413,7 +430,7 @@ __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const ui
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             float fx[8];
-            unpack8((t == 0 ? x0 : x1)[v], fx);
+            unpack8x<XH>((t == 0 ? x0 : x1)[v], fx);
 #pragma unroll
             for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
         }
@@ -422,7 +439,7 @@ __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const ui
 }
 
 // Gate and up rows against the same tokens.
-template <int NT>
+template <int NT, bool XH = false>
 __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const uint4* __restrict__ r3,
                                           const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nvec,
                                           int lane, float (&g)[NT], float (&u)[NT]) {
@@ -437,7 +454,7 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             float fx[8];
-            unpack8((t == 0 ? x0 : x1)[v], fx);
+            unpack8x<XH>((t == 0 ? x0 : x1)[v], fx);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 pg[t][e & 3] = fmaf(f1[e], fx[e], pg[t][e & 3]);
@@ -481,66 +498,115 @@ __device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rs
         for (int t = 0; t < NT; ++t) acc[j][t] = pa[j][t][0] + pa[j][t][1];
 }
 
-// One 32-element MXFP4 block (16 code bytes) against 32 bf16 values of each
-// token; returns the unscaled block sums.
-template <int NT>
-__device__ __forceinline__ void block_mxfp4(const uint4 q, const uint4* __restrict__ x0, const uint4* __restrict__ x1,
-                                            int b, float (&bs)[NT]) {
+// ---- MXFP4 with f16 block sums. The codes of a 32-element block become
+// f16 pairs by the hardware conversion; the activations are f16 scaled by a
+// power of two so that their magnitude stays below 256. Every product of an
+// e2m1 value (two significant bits) and such an activation (a bf16 value:
+// eight significant bits) is exact in f16, and a 32-term block sum stays
+// below 2^16; the block sum is accumulated in four f16 chains of eight
+// terms, then converted to fp32, scaled by the block's e8m0 scale (and the
+// activation's power of two) and accumulated in fp32.
+
+// Block sum of 16 code pairs against 16 activation pairs (four uint4).
+__device__ __forceinline__ float block_h(const uint32_t (&w)[16], const uint4 (&a)[4]) {
+    uint32_t c0 = 0u, c1 = 0u, c2 = 0u, c3 = 0u;
 #pragma unroll
-    for (int t = 0; t < NT; ++t) bs[t] = 0.f;
-    float pa[NT][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const uint32_t a = (&q.x)[w];
-        float d[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[e] = e2m1_to_f32(a >> (4 * e));
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float fx[8];
-            unpack8((t == 0 ? x0 : x1)[b * 4 + w], fx);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(d[e], fx[e], pa[t][e & 3]);
-        }
+    for (int k = 0; k < 4; ++k) {
+        c0 = hfma2(w[4 * k + 0], a[k].x, c0);
+        c1 = hfma2(w[4 * k + 1], a[k].y, c1);
+        c2 = hfma2(w[4 * k + 2], a[k].z, c2);
+        c3 = hfma2(w[4 * k + 3], a[k].w, c3);
     }
-    sum4<NT>(pa, bs);
+    const float2 f0 = f16x2_to_f32(c0), f1 = f16x2_to_f32(c1), f2 = f16x2_to_f32(c2), f3 = f16x2_to_f32(c3);
+    return ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
 }
 
-// MXFP4 gate and up rows: per block, the code sums times the e8m0 scale.
+__device__ __forceinline__ void decode_block(const uint4 q, uint32_t (&w)[16]) {
+    uint32_t t[4];
+    e2m1x8_to_f16x2(q.x, t);
+    w[0] = t[0], w[1] = t[1], w[2] = t[2], w[3] = t[3];
+    e2m1x8_to_f16x2(q.y, t);
+    w[4] = t[0], w[5] = t[1], w[6] = t[2], w[7] = t[3];
+    e2m1x8_to_f16x2(q.z, t);
+    w[8] = t[0], w[9] = t[1], w[10] = t[2], w[11] = t[3];
+    e2m1x8_to_f16x2(q.w, t);
+    w[12] = t[0], w[13] = t[1], w[14] = t[2], w[15] = t[3];
+}
+
+// MXFP4 gate and up rows against tokens held in f16 (times their power of
+// two, which the caller removes).
 template <int NT>
-__device__ __forceinline__ void dot2_mxfp4(const uint4* __restrict__ c1, const uint8_t* __restrict__ s1,
-                                           const uint4* __restrict__ c3, const uint8_t* __restrict__ s3,
-                                           const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nblk,
-                                           int lane, float (&g)[NT], float (&u)[NT]) {
+__device__ __forceinline__ void dot2_mxh(const uint4* __restrict__ c1, const uint8_t* __restrict__ s1,
+                                         const uint4* __restrict__ c3, const uint8_t* __restrict__ s3,
+                                         const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nblk,
+                                         int lane, float (&g)[NT], float (&u)[NT]) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
+#pragma unroll 2
     for (int b = lane; b < nblk; b += 32) {
-        float bg[NT], bu[NT];
-        block_mxfp4<NT>(c1[b], x0, x1, b, bg);
-        block_mxfp4<NT>(c3[b], x0, x1, b, bu);
+        uint32_t w1[16], w3[16];
+        decode_block(c1[b], w1);
+        decode_block(c3[b], w3);
         const float sc1 = e8m0_to_f32(s1[b]), sc3 = e8m0_to_f32(s3[b]);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            g[t] = fmaf(bg[t], sc1, g[t]);
-            u[t] = fmaf(bu[t], sc3, u[t]);
+            const uint4* xb = (t == 0 ? x0 : x1) + 4 * b;
+            const uint4 a[4] = {xb[0], xb[1], xb[2], xb[3]};
+            g[t] = fmaf(block_h(w1, a), sc1, g[t]);
+            u[t] = fmaf(block_h(w3, a), sc3, u[t]);
         }
     }
 }
 
-template <int NT, int STRIDE = 32>
-__device__ __forceinline__ void dot_mxfp4(const uint4* __restrict__ c, const uint8_t* __restrict__ s,
-                                          const uint4* __restrict__ h0, const uint4* __restrict__ h1, int nblk,
-                                          int lane, float (&acc)[NT]) {
+// One bf16 activation block (32 values, four uint4) as f16 times 2^s, s
+// chosen from the block's own largest magnitude; returns 2^-s.
+__device__ __forceinline__ float block_to_f16(const uint4* __restrict__ src, uint4 (&a)[4]) {
+    float f[32];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-    for (int b = lane; b < nblk; b += STRIDE) {
-        float bs[NT];
-        block_mxfp4<NT>(c[b], h0, h1, b, bs);
-        const float sc = e8m0_to_f32(s[b]);
+    for (int k = 0; k < 4; ++k) {
+        float t8[8];
+        unpack8(src[k], t8);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) acc[t] = fmaf(bs[t], sc, acc[t]);
+        for (int e = 0; e < 8; ++e) f[8 * k + e] = t8[e];
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fabsf(f[e]));
+    const int sh = f16_range_shift(mx);
+    const float sc = exp2i(sh);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        a[k].x = f32x2_to_f16x2(f[8 * k + 0] * sc, f[8 * k + 1] * sc);
+        a[k].y = f32x2_to_f16x2(f[8 * k + 2] * sc, f[8 * k + 3] * sc);
+        a[k].z = f32x2_to_f16x2(f[8 * k + 4] * sc, f[8 * k + 5] * sc);
+        a[k].w = f32x2_to_f16x2(f[8 * k + 6] * sc, f[8 * k + 7] * sc);
+    }
+    return exp2i(-sh);
+}
+
+// Four MXFP4 down rows (codes crow[j], scales srow[j]) against NT activation
+// vectors (bf16, converted block by block).
+template <int NT>
+__device__ __forceinline__ void dot4_mxh(const uint8_t* const (&crow)[4], const uint8_t* const (&srow)[4],
+                                         const uint4* __restrict__ h0, const uint4* __restrict__ h1, int nblk,
+                                         int lane, float (&acc)[4][NT]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[j][t] = 0.f;
+    for (int b = lane; b < nblk; b += 32) {
+        uint4 a[NT][4];
+        float inv[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) inv[t] = block_to_f16((t == 0 ? h0 : h1) + 4 * b, a[t]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[16];
+            decode_block(reinterpret_cast<const uint4*>(crow[j])[b], w);
+            const float sw = e8m0_to_f32(srow[j][b]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[j][t] = fmaf(block_h(w, a[t]) * inv[t], sw, acc[j][t]);
+        }
     }
 }
 
@@ -582,8 +648,9 @@ struct Consumer {
             for (int t = 0; t < p.M; ++t) {
                 float acc[1];
                 const uint4* xt = xrow(t);
-                dot_bf16<1>(row, xt, xt, nvec, lane, acc);
+                dot_bf16<1, 32, WFMT == 1>(row, xt, xt, nvec, lane, acc);
                 acc[0] = warp_sum(acc[0]);
+                if (WFMT == 1) acc[0] *= plan->x_inv[t];
                 if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
             }
         }
@@ -595,14 +662,14 @@ struct Consumer {
         if (WFMT == 0 || shared) {
             const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
-            dot2_bf16<NT>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
+            dot2_bf16<NT, WFMT == 1>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
         } else {
             const size_t cb = (size_t)p.H / 2, sbytes = (size_t)p.H / 32;
             const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
             const uint4* c3 = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
             const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
             const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
-            dot2_mxfp4<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
+            dot2_mxh<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
         }
     }
 
@@ -626,6 +693,10 @@ struct Consumer {
                 u[0] = warp_sum(u[0]);
                 g[1] = warp_sum(g[1]);
                 u[1] = warp_sum(u[1]);
+                if (WFMT == 1) {  // tokens are held times 2^s_t
+                    g[0] *= plan->x_inv[ta], u[0] *= plan->x_inv[ta];
+                    g[1] *= plan->x_inv[tb], u[1] *= plan->x_inv[tb];
+                }
                 if (lane < 2)
                     hdst[(size_t)(q0 + lane) * inter + j] =
                         f32_to_bf16_bits(silu_mul(lane ? g[1] : g[0], lane ? u[1] : u[0]));
@@ -636,25 +707,9 @@ struct Consumer {
                 gateup_group<1>(st, ch, j, ta, ta, shared, g, u);
                 g[0] = warp_sum(g[0]);
                 u[0] = warp_sum(u[0]);
+                if (WFMT == 1) g[0] *= plan->x_inv[ta], u[0] *= plan->x_inv[ta];
                 if (lane == 0) hdst[(size_t)q0 * inter + j] = f32_to_bf16_bits(silu_mul(g[0], u[0]));
             }
-        }
-    }
-
-    template <int NT>
-    __device__ __forceinline__ void down_group(const uint8_t* st, const Chunk& ch, int j, int qa, int qb, bool shared,
-                                               size_t sofs, float (&acc)[NT]) const {
-        const int inter = shared ? p.Is : p.I;
-        const size_t hb = (size_t)ch.np * inter * 2;
-        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)qa * inter * 2);
-        const uint4* hb_ = reinterpret_cast<const uint4*>(st + (size_t)qb * inter * 2);
-        if (WFMT == 0 || shared) {
-            const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * inter * 2);
-            dot_bf16<NT>(row, ha, hb_, inter / 8, lane, acc);
-        } else {
-            const uint4* row = reinterpret_cast<const uint4*>(st + hb + (size_t)j * (p.I / 2));
-            const uint8_t* sc = st + hb + (size_t)ch.n * (p.I / 2) + sofs + (size_t)j * (p.I / 32);
-            dot_mxfp4<NT>(row, sc, ha, hb_, p.I / 32, lane, acc);
         }
     }
 
@@ -738,25 +793,51 @@ struct Consumer {
                 }
                 continue;
             }
-            for (int r = ra; r < rb; ++r) {
-                const int j = r - ch.r0;
+            // MXFP4 routed rows, four at a time (rows past the part's end
+            // repeat its last row; their results are dropped)
+            const size_t hbytes = (size_t)ch.np * p.I * 2;
+            const uint8_t* codes = st + hbytes;
+            const uint8_t* scls = st + hbytes + (size_t)ch.n * (p.I / 2) + sofs;
+            const int nblk = p.I / 32;
+            for (int r = ra; r < rb; r += 4) {
+                const int nrow = min(4, rb - r);
+                const uint8_t* crow[4];
+                const uint8_t* srow[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = r - ch.r0 + min(jj, nrow - 1);
+                    crow[jj] = codes + (size_t)j * (p.I / 2);
+                    srow[jj] = scls + (size_t)j * nblk;
+                }
                 float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
                 int q0 = 0;
                 for (; q0 + 2 <= ch.np; q0 += 2) {
-                    float acc[2];
-                    down_group<2>(st, ch, j, q0, q0 + 1, shared, sofs, acc);
-                    acc[0] = warp_sum(acc[0]);
-                    acc[1] = warp_sum(acc[1]);
-                    if (lane == 0) {
-                        out[(size_t)q0 * p.rpc] = acc[0];
-                        out[(size_t)(q0 + 1) * p.rpc] = acc[1];
-                    }
+                    float acc[4][2];
+                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
+                    dot4_mxh<2>(crow, srow, ha, ha + p.I / 8, nblk, lane, acc);
+#pragma unroll
+                    for (int o = 16; o; o >>= 1)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
+                            acc[jj][1] += __shfl_xor_sync(0xffffffffu, acc[jj][1], o);
+                        }
+                    if (lane == 0)
+                        for (int jj = 0; jj < nrow; ++jj) {
+                            out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
+                            out[(size_t)(q0 + 1) * p.rpc + jj] = acc[jj][1];
+                        }
                 }
                 if (q0 < ch.np) {
-                    float acc[1];
-                    down_group<1>(st, ch, j, q0, q0, shared, sofs, acc);
-                    acc[0] = warp_sum(acc[0]);
-                    if (lane == 0) out[(size_t)q0 * p.rpc] = acc[0];
+                    float acc[4][1];
+                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
+                    dot4_mxh<1>(crow, srow, ha, ha, nblk, lane, acc);
+#pragma unroll
+                    for (int o = 16; o; o >>= 1)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
+                    if (lane == 0)
+                        for (int jj = 0; jj < nrow; ++jj) out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
                 }
             }
         }
@@ -981,7 +1062,38 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
-            for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+            if (WFMT == 0) {
+                for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+            } else {
+                // MXFP4 layers hold the tokens in f16 times 2^s_t, s_t chosen
+                // from the token's largest magnitude (exact for bf16 values
+                // in f16's normal range)
+                const int nvt = p.H / 8;
+                for (int t = warp; t < p.M; t += NCW) {
+                    float mx = 0.f;
+                    for (int i = lane; i < nvt; i += 32) {
+                        float f[8];
+                        unpack8(__ldg(src + (size_t)t * nvt + i), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(f[e]));
+                    }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    const int sh = f16_range_shift(mx);
+                    const float sc = exp2i(sh);
+                    for (int i = lane; i < nvt; i += 32) {
+                        float f[8];
+                        unpack8(__ldg(src + (size_t)t * nvt + i), f);
+                        uint4 v;
+                        v.x = f32x2_to_f16x2(f[0] * sc, f[1] * sc);
+                        v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
+                        v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
+                        v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
+                        dst[(size_t)t * nvt + i] = v;
+                    }
+                    if (lane == 0) plan->x_inv[t] = exp2i(-sh);
+                }
+            }
             if (!has_route)
                 for (int i = tid; i < p.M * p.k; i += NCT) {
                     plan->sel_e[i] = p.idx_in[i];

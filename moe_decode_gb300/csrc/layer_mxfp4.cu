@@ -16,9 +16,10 @@ __global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ codes, const ui
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / K;
         const int c = (int)(i - r * K);
-        const uint32_t byte = codes[r * (K / 2) + c / 2];
-        const uint32_t nib = (c & 1) ? (byte >> 4) : (byte & 15u);
-        out[i] = e2m1_to_f32(nib) * e8m0_to_f32(scales[r * (K / 32) + c / 32]);
+        uint32_t w[4];
+        e2m1x8_to_f16x2(codes[r * (K / 2) + c / 2], w);  // the kernels' decode
+        const float2 v = f16x2_to_f32(w[0]);
+        out[i] = ((c & 1) ? v.y : v.x) * e8m0_to_f32(scales[r * (K / 32) + c / 32]);
     }
 }
 

@@ -6,9 +6,9 @@
 namespace moe {
 
 // Consumer warps per CTA for each routed-weight format; one producer warp
-// comes on top. The totals (12 and 8 warps) spread evenly over the SM's four
-// schedulers, which keeps the per-thread register budget at 168 and 255.
-constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 11 : 7; }
+// comes on top. The total (12 warps) spreads evenly over the SM's four
+// schedulers and keeps the per-thread register budget at 168.
+constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 11 : 11; }
 constexpr int block_threads(int wfmt) { return (consumer_warps(wfmt) + 1) * 32; }
 constexpr uint32_t kStageBytes = 32768;               // one ring stage
 constexpr int kMaxStages = 6;
@@ -68,6 +68,8 @@ struct Plan {
     float pair_w[kMaxEntries];
     int16_t slot_e[kMaxEntries];    // distinct routed experts, ascending
     int16_t slot_p0[kMaxEntries + 1];
+    float x_inv[kMaxM];             // MXFP4 layers: tokens are held in f16 times
+                                    // 2^s_t; x_inv[t] = 2^-s_t
     int32_t nslot;
     int32_t npairs;
     int32_t abort;

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace moe {
 
@@ -135,13 +136,40 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
 }
 
 // ---------------------------------------------------------------- MXFP4
-// e2m1 magnitude code m (3 bits) placed in fp32 bits [24:22] reads as
-// 2^(e-127) * (1 + mant/2) for e = m >> 1 > 0 and as the subnormal
-// mant * 2^-127 for e = 0; scaling by 2^126 gives exactly the e2m1 value
-// (0, .5, 1, 1.5, 2, 3, 4, 6). Needs no flush-to-zero (the default).
-__device__ __forceinline__ float e2m1_to_f32(uint32_t nib) {
-    float mag = __uint_as_float((nib & 7u) << 22) * 0x1p126f;
-    return __uint_as_float(__float_as_uint(mag) | ((nib & 8u) << 28));
+// Eight e2m1 codes (one 32-bit word; element 2j in the low nibble of byte j)
+// to four f16 pairs with the hardware conversion: w[j] holds elements 2j (low
+// half) and 2j + 1 (high half). Every e2m1 value is exact in f16.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t v, uint32_t (&w)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "r"(v));
+}
+
+// ---------------------------------------------------------------- f16x2
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
+                        *reinterpret_cast<const __half2*>(&c));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t v) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+// (lo, hi) rounded to nearest into one f16 pair (lo in the low half).
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// 2^e as an fp32 for -126 <= e <= 127.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+// Power-of-two exponent s such that mx * 2^s lies in [128, 256) (mx > 0
+// normal), clamped to [-100, 100]; 0 for mx == 0.
+__device__ __forceinline__ int f16_range_shift(float mx) {
+    if (!(mx > 0.f)) return 0;
+    const int e = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+    return max(-100, min(100, 7 - e));
 }
 
 // 2^(s-127) for an e8m0 byte s (s = 0 is the subnormal 2^-127; s = 255 NaN).
