@@ -52,6 +52,12 @@ def _load():
         lib.oracle_mxfp4_value.restype = ctypes.c_float
         lib.oracle_mxfp4_decode.argtypes = [P, P, i64, i32, P]
         lib.oracle_route.argtypes = [P, i32, i32, P, i32, i32, i32, P, P, P]
+        lib.oracle_fp8_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_fp8_e4m3_value.restype = ctypes.c_double
+        lib.oracle_fp8_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_fp8_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_fp8_quantize.argtypes = [P, i64, i32, i32, P, P]
+        lib.oracle_lm_head.argtypes = [P, i32, i32, P, P, i32, i32, i32, P]
         lib.oracle_expert.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, i32, P]
         lib.oracle_ffn.argtypes = [P, i32, i32, P, P, i32, i32, i32, i32,
                                    P, P, P, P, P, P, i32, P, P, P, i32, P]
@@ -160,3 +166,37 @@ def ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict, E: int, I:
     if rc:
         raise ValueError(f"oracle_ffn rc={rc}")
     return y
+
+
+def fp8_e4m3_value(code: int) -> float:
+    return float(_load().oracle_fp8_e4m3_value(code & 0xFF))
+
+
+def fp8_e4m3_encode(v: float) -> int:
+    return int(_load().oracle_fp8_e4m3_encode(float(v)))
+
+
+def fp8_quantize(w_u16: np.ndarray, block: int):
+    """bf16 bits [R, K] -> (e4m3 codes u8 [R, K], fp32 scales [R, K / block])."""
+    w = _c(w_u16, np.uint16)
+    R, K = w.shape
+    codes = np.empty((R, K), np.uint8)
+    scales = np.empty((R, K // block), np.float32)
+    rc = _load().oracle_fp8_quantize(_ptr(w), R, K, block, _ptr(codes), _ptr(scales))
+    if rc:
+        raise ValueError(f"oracle_fp8_quantize: {rc}")
+    return codes, scales
+
+
+def lm_head(x_u16: np.ndarray, W, V: int, wfmt: int = 0, scale=None, acc_double: bool = False) -> np.ndarray:
+    """logits fp32 [M, V] of tokens x (bf16 bits [M, H]) against W (bf16 bits
+    [V, H], or e4m3 codes [V, H] with fp32 per-row scale for wfmt 2)."""
+    x = _c(x_u16, np.uint16)
+    M, H = x.shape
+    Wc = _c(W, np.uint16 if wfmt == 0 else np.uint8)
+    sc = None if scale is None else _c(scale, np.float32)
+    out = np.empty((M, V), np.float32)
+    rc = _load().oracle_lm_head(_ptr(x), M, H, _ptr(Wc), _ptr(sc), V, wfmt, int(acc_double), _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_lm_head: {rc}")
+    return out

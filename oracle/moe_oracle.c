@@ -243,3 +243,87 @@ int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
     free(xt); free(z); free(acc);
     return rc;
 }
+
+/* ------------------------------------------------------------------ FP8 */
+/* OCP "OCP 8-bit Floating Point Specification (OFP8)", format E4M3. */
+double oracle_fp8_e4m3_value(uint8_t code) {
+    const int sign = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+uint8_t oracle_fp8_e4m3_encode(float v) {
+    if (isnan(v)) return 0x7f;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const double a = fabs((double)v);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+    /* non-negative finite codes 0x00..0x7e have increasing values: take the
+       nearest, ties to the even code */
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c <= 0x7e; ++c) {
+        const double d = fabs(oracle_fp8_e4m3_value((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+int oracle_fp8_quantize(const uint16_t* w, int64_t R, int K, int block,
+                        uint8_t* codes, float* scales) {
+    if (!w || !codes || !scales || R < 0 || K <= 0 || block <= 0 || K % block) return -1;
+    const int nb = K / block;
+    for (int64_t r = 0; r < R; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* src = w + r * K + (int64_t)b * block;
+            float amax = 0.0f;
+            for (int i = 0; i < block; ++i) {
+                const float a = fabsf(oracle_bf16_to_f32(src[i]));
+                if (a > amax) amax = a;
+            }
+            const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[r * nb + b] = sc;
+            for (int i = 0; i < block; ++i)
+                codes[r * K + (int64_t)b * block + i] = oracle_fp8_e4m3_encode(oracle_bf16_to_f32(src[i]) / sc);
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ lm_head */
+/* "Chasing the Batch-1 Floor: Ling-3.0-flash Speculative Decode on
+   Blackwell", section "bf16 router gate and lm_head"; "3 ways to boost MoE
+   inference on NVIDIA DGX Spark", "Optimization 2: Online FP8 LM head
+   quantization" (FP8 weights of the output layer). */
+int oracle_lm_head(const uint16_t* x, int M, int H, const void* W,
+                   const float* scale, int V, int wfmt, int acc_double,
+                   float* logits) {
+    if (!x || !W || !logits || M < 0 || H <= 0 || V < 0) return -1;
+    if (wfmt != 0 && wfmt != 2) return -1;
+    if (wfmt == 2 && !scale) return -1;
+    for (int t = 0; t < M; ++t)
+        for (int v = 0; v < V; ++v) {
+            double accd = 0.0;
+            float accf = 0.0f;
+            for (int h = 0; h < H; ++h) {
+                const float xv = oracle_bf16_to_f32(x[(int64_t)t * H + h]);
+                double wv;
+                if (wfmt == 0)
+                    wv = oracle_bf16_to_f32(((const uint16_t*)W)[(int64_t)v * H + h]);
+                else
+                    wv = oracle_fp8_e4m3_value(((const uint8_t*)W)[(int64_t)v * H + h]) * (double)scale[v];
+                if (acc_double)
+                    accd += (double)xv * wv;
+                else
+                    accf += xv * (float)wv;
+            }
+            logits[(int64_t)t * V + v] = acc_double ? (float)accd : accf;
+        }
+    return 0;
+}

@@ -46,6 +46,30 @@ float oracle_mxfp4_value(uint8_t code, uint8_t scale);
 int oracle_mxfp4_decode(const uint8_t* codes, const uint8_t* scales,
                         int64_t rows, int K, float* out);
 
+/* Value of one FP8 e4m3 code (OCP 8-bit floating point, E4M3: sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent 0 encodes the
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no infinities; the
+ * largest finite magnitude is 448). */
+double oracle_fp8_e4m3_value(uint8_t code);
+
+/* The e4m3 code nearest to v (ties to the code with an even mantissa),
+ * saturating to +-448; NaN -> 0x7f; the sign of zero is kept. */
+uint8_t oracle_fp8_e4m3_encode(float v);
+
+/* Quantises bf16 rows [R, K] to e4m3 with one fp32 scale per block of
+ * `block` consecutive elements of a row (K % block == 0): scale =
+ * amax(block) / 448 in fp32 (1 for an all-zero block); code =
+ * encode(w / scale), the quotient in fp32. scales is [R, K / block]. */
+int oracle_fp8_quantize(const uint16_t* w, int64_t R, int K, int block,
+                        uint8_t* codes, float* scales);
+
+/* Output layer: logits[t, v] = sum_h x[t, h] * W[v, h] for M tokens and V
+ * rows. wfmt 0: W bf16 [V, H]; wfmt 2: W e4m3 codes [V, H] whose value is
+ * e4m3(code) * scale[v] (one fp32 scale per row). logits fp32 [M, V]. */
+int oracle_lm_head(const uint16_t* x, int M, int H, const void* W,
+                   const float* scale, int V, int wfmt, int acc_double,
+                   float* logits);
+
 /* Router: logits[t,e] = x[t,:] . Wg[e,:]; softmax over all E; the k largest
  * logits (ties: lower expert index first), in descending order; weights are
  * the selected probabilities renormalised to sum to one.
