@@ -46,6 +46,15 @@ WORKLOADS = {
 }
 
 
+# output layer (lm_head): the model's 157,184 x 2,560 vocabulary matrix (805 MB
+# in bf16, already far above L2: one copy is cold at every step)
+LM_WORKLOADS = {
+    "lmhead_bf16_m1": dict(M=1, wfmt=0, V=157184, H=2560),
+    "lmhead_fp8_m1": dict(M=1, wfmt=2, V=157184, H=2560),
+    "lmhead_bf16_m6": dict(M=6, wfmt=0, V=157184, H=2560),
+}
+
+
 def layer_shape(name: str):
     from moe_decode_gb300 import synth
     E = WORKLOADS[name].get("E", synth.LING.n_experts)
@@ -231,6 +240,43 @@ class Workload:
         return sum(self.step_bytes(s) for s in range(K)) / K
 
 
+class LmWorkload:
+    """Output-layer GEMV: logits [M, V] of M tokens (one launch per step)."""
+
+    def __init__(self, name: str, device):
+        from moe_decode_gb300 import api, synth
+        self.api = api
+        self.name = name
+        w = LM_WORKLOADS[name]
+        self.M, self.wfmt, self.V, self.H = w["M"], w["wfmt"], w["V"], w["H"]
+        Wb = synth.normal_bf16(3000, 1, 0, self.V * self.H, synth.WEIGHT_SIGMA, device).view(self.V, self.H)
+        if self.wfmt == 0:
+            self.W, self.scale = Wb, None
+        else:
+            self.W = torch.empty((self.V, self.H), dtype=torch.uint8, device=device)
+            self.scale = torch.empty((self.V, 1), dtype=torch.float32, device=device)
+            api.fp8_quantize(Wb, self.H, self.W, self.scale)
+            del Wb
+        self.xs = torch.stack([synth.x_independent(synth.LING, s, self.M, device=device) for s in range(PERIOD)])
+        self.logits = torch.empty((self.M, self.V), dtype=torch.float32, device=device)
+        self.ws = torch.empty(api.LM_HEAD_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+        api.workspace_init(self.ws)
+        self.weight_bytes = self.W.numel() * self.W.element_size()
+        self.distinct = np.zeros(1)
+
+    def step(self, s: int, stream, idx=None, w=None, x=None, y=None):
+        self.api.lm_head(self.xs[s % PERIOD] if x is None else x, self.W, self.V, self.H, self.logits, self.ws,
+                         wfmt=self.wfmt, w_scale=None if self.scale is None else self.scale.view(-1), stream=stream)
+
+    def routing_pass(self, stream):
+        self.step(0, stream)
+        stream.synchronize()
+
+    def mean_bytes(self, K: int) -> float:
+        """Weights (+ e4m3 row scales), tokens in, logits out."""
+        return self.weight_bytes + (self.V * 4 if self.wfmt else 0) + self.M * self.H * 2 + self.M * self.V * 4
+
+
 def capture_graph(wl: Workload, start: int, n: int, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -368,7 +414,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="ling_m1")
-    ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6",
+    ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6",
                     help="comma-separated extra workloads measured in the same run ('' for none)")
     ap.add_argument("--cpu-steps", type=int, default=0,
                     help="oracle steps timed for cpu_baseline (0: about 12 s of oracle work for the workload)")
@@ -404,7 +450,7 @@ def main():
     results = {}
     names = [args.workload] + [n for n in args.also.split(",") if n and n != args.workload]
     for name in names:
-        wl = Workload(name, device)
+        wl = LmWorkload(name, device) if name in LM_WORKLOADS else Workload(name, device)
         wl.routing_pass(stream)
         main_run = name == args.workload
         sampler = ClockSampler(visible_gpu_index(local_rank)) if main_run else None

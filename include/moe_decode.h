@@ -184,6 +184,39 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg,
                                     float* w_out, void* y, uint32_t flags,
                                     void* stream);
 
+/* ------------------------------------------------------------ output layer
+ * Output layer (lm_head) GEMV for M = 1..16 tokens: logits fp32 [M, V] =
+ * x bf16 [M, H] . W^T. "Chasing the Batch-1 Floor: Ling-3.0-flash
+ * Speculative Decode on Blackwell", "bf16 router gate and lm_head"; "3 ways
+ * to boost MoE inference on NVIDIA DGX Spark", "Optimization 2: Online FP8
+ * LM head quantization" (157,184 x 2,560 for the model).
+ *  wfmt 0: W bf16 [V, H] (H a multiple of 8), w_scale unused (may be NULL).
+ *  wfmt 2: W FP8 e4m3 codes [V, H] (H a multiple of 16) and w_scale fp32 [V],
+ *          one scale per row: W[v, h] = e4m3(code) * w_scale[v] (see
+ *          moe_fp8_quantize with block = H). Activations stay bf16.
+ * H <= 8192. Every weight byte is read once per call. ws: a device buffer of
+ * at least MOE_LM_HEAD_WORKSPACE_BYTES (status word; zero it once with
+ * moe_workspace_init; moe_read_status reads it). flags: MOE_F_NO_PDL. One
+ * launch; errors as for the layer calls. */
+#define MOE_LM_HEAD_WORKSPACE_BYTES 1024u
+int moe_lm_head(const void* x, int M, const void* W, const float* w_scale,
+                int V, int H, int wfmt, float* logits, void* ws,
+                size_t ws_bytes, uint32_t flags, void* stream);
+
+/* FP8 e4m3 quantisation of bf16 rows [rows, K] with one fp32 scale per
+ * block of `block` consecutive elements of a row (block a multiple of 32
+ * dividing K): scale = amax(block) / 448 (1 for an all-zero block), code =
+ * the e4m3 value nearest to w / scale (ties to even, saturating). codes u8
+ * [rows, K], scales fp32 [rows, K / block] (all device). Not on the hot
+ * path: it prepares weights for moe_lm_head. */
+int moe_fp8_quantize(const void* w, int64_t rows, int K, int block,
+                     uint8_t* codes, float* scales, void* stream);
+
+/* Decodes e4m3 rows with the kernels' conversion: out fp32 [rows, K] =
+ * e4m3(code) * scale[row, col / block] (all device). */
+int moe_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows,
+                    int K, int block, float* out, void* stream);
+
 /* Synchronises `stream`, then copies the device status word of `ws` to
  * *dev_status (MOE_OK or a device code above). Not for the hot path. */
 int moe_read_status(const void* ws, void* stream, int32_t* dev_status);

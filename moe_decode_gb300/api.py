@@ -27,6 +27,7 @@ F_DEBUG_FORCE_TIMEOUT = 256
 OPT_GRID_CTAS = 1
 OPT_WAIT_TIMEOUT_NS = 2
 OPT_TRACE_BUFFER = 3
+LM_HEAD_WORKSPACE_BYTES = 1024
 STATIC_SCRATCH_BYTES = 524288
 
 
@@ -65,9 +66,13 @@ def _load():
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_mxfp4_dequant.argtypes = [P, P, I64, I32, P, P]
     lib.moe_set_option.argtypes = [I32, I64]
+    lib.moe_lm_head.argtypes = [P, I32, P, P, I32, I32, I32, P, P, SZ, ctypes.c_uint32, P]
+    lib.moe_fp8_quantize.argtypes = [P, I64, I32, I32, P, P, P]
+    lib.moe_fp8_dequant.argtypes = [P, P, I64, I32, I32, P, P]
     lib.moe_last_launch_count.argtypes = []
     for f in ("moe_workspace_init", "moe_route", "moe_ffn", "moe_decode_layer", "moe_decode_layer_static_scratch",
-              "moe_read_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count"):
+              "moe_read_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count",
+              "moe_lm_head", "moe_fp8_quantize", "moe_fp8_dequant"):
         getattr(lib, f).restype = I32
     return lib
 
@@ -179,3 +184,22 @@ def set_option(option: int, value: int):
 
 def last_launch_count() -> int:
     return int(lib.moe_last_launch_count())
+
+
+def lm_head(x, W, V: int, H: int, logits, ws, wfmt: int = 0, w_scale=None, flags: int = 0, stream=None):
+    """logits fp32 [M, V] = x bf16 [M, H] . W^T; W bf16 [V, H] (wfmt 0) or e4m3
+    codes u8 [V, H] with fp32 per-row scales w_scale [V] (wfmt 2)."""
+    _check(lib.moe_lm_head(_ptr(x), x.shape[0], _ptr(W), _ptr(w_scale), V, H, wfmt, _ptr(logits), _ptr(ws),
+                           ws.numel(), flags, _stream(stream)), "moe_lm_head")
+
+
+def fp8_quantize(w, block: int, codes, scales, stream=None):
+    rows, K = w.shape
+    _check(lib.moe_fp8_quantize(_ptr(w), rows, K, block, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_fp8_quantize")
+
+
+def fp8_dequant(codes, scales, block: int, out, stream=None):
+    rows, K = codes.shape
+    _check(lib.moe_fp8_dequant(_ptr(codes), _ptr(scales), rows, K, block, _ptr(out), _stream(stream)),
+           "moe_fp8_dequant")

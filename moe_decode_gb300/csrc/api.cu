@@ -315,6 +315,78 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     return launch(p, shape->wfmt, st, (flags & MOE_F_NO_PDL) == 0, dev);
 }
 
+int moe_lm_head(const void* x, int M, const void* W, const float* w_scale, int V, int H, int wfmt, float* logits,
+                void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+    g_last_launches = 0;
+    if (M < 1 || M > moe::kMaxM) return MOE_EM;
+    if (wfmt != 0 && wfmt != 2) return MOE_ESHAPE;
+    if (V < 1 || H <= 0 || H > 8192 || H % (wfmt == 0 ? 8 : 16) != 0) return MOE_ESHAPE;
+    if (flags & ~MOE_F_NO_PDL) return MOE_EINVAL;
+    if (!x || !W || !logits || (wfmt == 2 && !w_scale)) return MOE_EINVAL;
+    if (!aligned16(x) || !aligned16(W)) return MOE_EALIGN;
+    if (!ws) return MOE_EWORKSPACE;
+    if (!aligned16(ws)) return MOE_EALIGN;
+    if (ws_bytes < MOE_LM_HEAD_WORKSPACE_BYTES) return MOE_EWORKSPACE;
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc) return rc;
+    moe::LmParams p = {};
+    p.x = static_cast<const uint16_t*>(x);
+    p.W = static_cast<const uint8_t*>(W);
+    p.scale = w_scale;
+    p.logits = logits;
+    p.ctrl = static_cast<unsigned*>(ws);
+    p.M = M;
+    p.H = H;
+    p.V = V;
+    p.G = g_opt.grid_ctas > 0 ? g_opt.grid_ctas : dev.sms;
+    if (p.G > dev.sms) return MOE_EINVAL;
+    p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
+    const size_t bar_bytes = 128, x_bytes = align_up((size_t)M * H * 2, 128);
+    if ((size_t)dev.smem_optin <= bar_bytes + x_bytes) return MOE_ESHAPE;
+    int ns = (int)(((size_t)dev.smem_optin - bar_bytes - x_bytes) / moe::kStageBytes);
+    if (ns > moe::kMaxStages) ns = moe::kMaxStages;
+    if (ns < 2) return MOE_ESHAPE;
+    p.ns = ns;
+    p.off_bar = (uint32_t)(ns * moe::kStageBytes);
+    p.off_x = p.off_bar + (uint32_t)bar_bytes;
+    p.smem_bytes = p.off_x + (uint32_t)x_bytes;
+    if (moe::launch_lm_head(p, wfmt, static_cast<cudaStream_t>(stream), (flags & MOE_F_NO_PDL) == 0) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
+    g_last_launches = 1;
+    return MOE_OK;
+}
+
+int moe_fp8_quantize(const void* w, int64_t rows, int K, int block, uint8_t* codes, float* scales, void* stream) {
+    g_last_launches = 0;
+    if (!w || !codes || !scales) return MOE_EINVAL;
+    if (rows < 0 || K <= 0 || block <= 0 || block % 32 != 0 || K % block != 0) return MOE_ESHAPE;
+    if (moe::launch_fp8_quantize(static_cast<const uint16_t*>(w), rows, K, block, codes, scales,
+                                 static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
+    g_last_launches = rows > 0 ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows, int K, int block, float* out,
+                    void* stream) {
+    g_last_launches = 0;
+    if (!codes || !scales || !out) return MOE_EINVAL;
+    if (rows < 0 || K <= 0 || block <= 0 || K % block != 0) return MOE_ESHAPE;
+    if (moe::launch_fp8_dequant(codes, scales, rows, K, block, out, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
+    g_last_launches = rows > 0 ? 1 : 0;
+    return MOE_OK;
+}
+
 int moe_read_status(const void* ws, void* stream, int32_t* dev_status) {
     if (!ws || !dev_status) return MOE_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,308 @@
+// Output layer (lm_head) for batch-1 decode and speculative verify:
+// logits[t, v] = x_t . W[v] for M <= 16 tokens over a V x H weight matrix,
+// bf16 or FP8 e4m3 with one scale per row, and the FP8 quantiser and decode
+// that go with it.
+//
+// "Chasing the Batch-1 Floor: Ling-3.0-flash Speculative Decode on
+// Blackwell", section "bf16 router gate and lm_head" (the output GEMV is
+// weight-bandwidth bound at batch 1); "3 ways to boost MoE inference on
+// NVIDIA DGX Spark", "Optimization 2: Online FP8 LM head quantization" (the
+// 157,184 x 2,560 vocabulary matrix stored in FP8 to halve its reads).
+//
+// A persistent kernel, one CTA per SM: CTA c owns the rows [cV/G, (c+1)V/G)
+// and streams them once, in 32 KB bulk copies, through a ring of shared
+// memory stages (one producer lane, full/empty mbarriers); each consumer
+// warp takes whole rows against all M tokens. Every wait is bounded; a wait
+// that runs out sets MOE_ETIMEOUT in the status word and the CTA stops.
+#include "launch.h"
+#include "layer_params.h"
+#include "lm_params.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr uint32_t LSB = kStageBytes;
+
+__device__ __forceinline__ bool lm_aborted(const volatile int* flag) { return *flag != 0; }
+
+__device__ __forceinline__ void lm_abort(const LmParams& p, volatile int* flag) {
+    atomicCAS(reinterpret_cast<int*>(p.ctrl + kCtlStatus), 0, -101 /* MOE_ETIMEOUT */);
+    *flag = 1;
+}
+
+__device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, const LmParams& p, volatile int* flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (lm_aborted(flag)) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            lm_abort(p, flag);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ float lm_warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Two e4m3 codes (a 16-bit half-word; element 2j in the low byte) to an f16
+// pair with the hardware conversion (every e4m3 value is exact in f16).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(v));
+}
+
+// Sixteen e4m3 codes (one uint4) as fp32.
+__device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t lo, hi;
+        e4m3x4_to_f16x2(w[k], lo, hi);
+        const float2 a = f16x2_to_f32(lo), b = f16x2_to_f32(hi);
+        f[4 * k + 0] = a.x;
+        f[4 * k + 1] = a.y;
+        f[4 * k + 2] = b.x;
+        f[4 * k + 3] = b.y;
+    }
+}
+
+// acc[t] = row . x_t over H elements; this lane takes 16-byte weight vectors
+// lane, lane + 32, ... (bf16: 8 elements, e4m3: 16 elements per vector).
+template <int WT, int NT>
+__device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint4* __restrict__ x0,
+                                       const uint4* __restrict__ x1, int H, int lane, float (&acc)[NT]) {
+    float pa[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
+    if (WT == 0) {
+        const int nvec = H / 8;
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            float fw[8];
+            unpack8(row[v], fw);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float fx[8];
+                unpack8((t == 0 ? x0 : x1)[v], fx);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
+            }
+        }
+    } else {
+        const int nvec = H / 16;
+#pragma unroll 2
+        for (int v = lane; v < nvec; v += 32) {
+            float fw[16];
+            unpack16_e4m3(row[v], fw);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4* xt = t == 0 ? x0 : x1;
+                float fa[8], fb[8];
+                unpack8(xt[2 * v], fa);
+                unpack8(xt[2 * v + 1], fb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    pa[t][e & 3] = fmaf(fw[e], fa[e], pa[t][e & 3]);
+                    pa[t][e & 3] = fmaf(fw[8 + e], fb[e], pa[t][e & 3]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0] + pa[t][1]) + (pa[t][2] + pa[t][3]);
+}
+
+template <int WT>
+__global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_constant__ LmParams p) {
+    constexpr int NCW = kLmConsumerWarps;
+    constexpr int NCT = NCW * 32;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bars = smem_u32(smem + p.off_bar);
+    volatile int* flag = reinterpret_cast<volatile int*>(smem + p.off_bar + 2 * p.ns * 8);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + p.off_x);
+    if (tid == 0) {
+        for (int i = 0; i < p.ns; ++i) {
+            mbar_init(bars + i * 8, 1);
+            mbar_init(bars + (p.ns + i) * 8, NCW);
+        }
+        *flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int c = (int)blockIdx.x;
+    const int v0 = (int)((int64_t)c * p.V / p.G), v1 = (int)((int64_t)(c + 1) * p.V / p.G);
+    const uint32_t rowbytes = (uint32_t)p.H * (WT == 0 ? 2u : 1u);
+    const int cap = (int)(LSB / rowbytes);
+    const uint32_t base = smem_u32(smem);
+
+    if (warp == NCW) {
+        if (lane == 0) {
+            // the weights depend on no earlier launch: stream them at once
+            const uint64_t pol = policy_evict_first();
+            uint32_t n = 0, s = 0, ph = 0;
+            bool ok = true;
+            for (int r = v0; r < v1 && ok; r += cap, ++n) {
+                const int nr = min(cap, v1 - r);
+                if (n >= (uint32_t)p.ns) ok = lm_wait(bars + (p.ns + s) * 8, ph ^ 1u, p, flag);
+                if (!ok) break;
+                const uint32_t b = (uint32_t)nr * rowbytes;
+                mbar_arrive_expect_tx(bars + s * 8, b);
+                bulk_g2s(base + s * LSB, p.W + (size_t)r * rowbytes, b, bars + s * 8, pol);
+                if (++s == (uint32_t)p.ns) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                const uint32_t lo = n > (uint32_t)p.ns ? n - p.ns : 0;
+                for (uint32_t i = lo; i < n; ++i) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(bars + (i % p.ns) * 8, (i / p.ns) & 1u))
+                        if (global_timer_ns() - t0 > p.timeout_ns) break;
+                }
+            }
+        }
+    } else {
+        pdl_wait();
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(p.x);
+            uint4* dst = reinterpret_cast<uint4*>(xs);
+            const int nv = p.M * p.H / 8;
+            for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+        }
+        named_bar_sync(1, NCT);
+        uint32_t s = 0, ph = 0;
+        int q = 0;
+        const int nvx = p.H / 8;
+        for (int r = v0; r < v1; r += cap) {
+            const int nr = min(cap, v1 - r);
+            if (!lm_wait(bars + s * 8, ph, p, flag)) break;
+            const uint8_t* st = reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(base + s * LSB));
+            for (int j = 0; j < nr; ++j, ++q) {
+                if (q % NCW != warp) continue;
+                const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * rowbytes);
+                const float sc = WT == 0 ? 1.f : __ldg(p.scale + r + j);
+                int t = 0;
+                for (; t + 2 <= p.M; t += 2) {
+                    float acc[2];
+                    const uint4* xa = reinterpret_cast<const uint4*>(xs) + (size_t)t * nvx;
+                    lm_dot<WT, 2>(row, xa, xa + nvx, p.H, lane, acc);
+                    acc[0] = lm_warp_sum(acc[0]);
+                    acc[1] = lm_warp_sum(acc[1]);
+                    if (lane == 0) {
+                        p.logits[(size_t)t * p.V + r + j] = acc[0] * sc;
+                        p.logits[(size_t)(t + 1) * p.V + r + j] = acc[1] * sc;
+                    }
+                }
+                if (t < p.M) {
+                    float acc[1];
+                    const uint4* xa = reinterpret_cast<const uint4*>(xs) + (size_t)t * nvx;
+                    lm_dot<WT, 1>(row, xa, xa, p.H, lane, acc);
+                    acc[0] = lm_warp_sum(acc[0]);
+                    if (lane == 0) p.logits[(size_t)t * p.V + r + j] = acc[0] * sc;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + (p.ns + s) * 8);
+            if (++s == (uint32_t)p.ns) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    }
+}
+
+// e4m3 quantisation of bf16 rows: one warp per (row, block); scale =
+// amax / 448 in fp32 (1 for an all-zero block), code = nearest e4m3 to
+// w / scale (ties to even, saturating), by the hardware conversion.
+__global__ void fp8_quantize_kernel(const uint16_t* __restrict__ w, int64_t rows, int K, int block,
+                                    uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    const int nb = K / block;
+    const int64_t units = rows * nb;
+    const int lane = threadIdx.x & 31;
+    for (int64_t u = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; u < units;
+         u += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+        const int64_t r = u / nb;
+        const int b = (int)(u - r * nb);
+        const uint16_t* src = w + r * K + (int64_t)b * block;
+        float amax = 0.f;
+        for (int i = lane; i < block; i += 32) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[i] << 16)));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        if (lane == 0) scales[u] = sc;
+        uint8_t* dst = codes + r * K + (int64_t)b * block;
+        for (int i = 2 * lane; i < block; i += 64) {
+            const float a = __uint_as_float((uint32_t)src[i] << 16) / sc;
+            const float bb = __uint_as_float((uint32_t)src[i + 1] << 16) / sc;
+            uint16_t pr;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pr) : "f"(bb), "f"(a));
+            *reinterpret_cast<uint16_t*>(dst + i) = pr;
+        }
+    }
+}
+
+// e4m3 decode with the kernels' conversion: out = e4m3(code) * scale.
+__global__ void fp8_dequant_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                                   int64_t rows, int K, int block, float* __restrict__ out) {
+    const int64_t n = rows * (int64_t)K;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / K;
+        const int col = (int)(i - r * K);
+        uint32_t lo, hi;
+        e4m3x4_to_f16x2(codes[i], lo, hi);
+        out[i] = f16x2_to_f32(lo).x * scales[r * (K / block) + col / block];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_lm_head(const LmParams& p, int wt, cudaStream_t stream, bool pdl) {
+    void (*kern)(LmParams) = wt == 0 ? lm_head_kernel<0> : lm_head_kernel<2>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.G);
+    cfg.blockDim = dim3(kLmThreads);
+    cfg.dynamicSmemBytes = p.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_fp8_quantize(const uint16_t* w, int64_t rows, int K, int block, uint8_t* codes, float* scales,
+                                cudaStream_t stream) {
+    const int64_t units = rows * (K / block);
+    if (units == 0) return cudaSuccess;
+    int blocks = (int)((units * 32 + 255) / 256);
+    if (blocks > 8192) blocks = 8192;
+    fp8_quantize_kernel<<<blocks, 256, 0, stream>>>(w, rows, K, block, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows, int K, int block, float* out,
+                               cudaStream_t stream) {
+    const int64_t n = rows * (int64_t)K;
+    if (n == 0) return cudaSuccess;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    fp8_dequant_kernel<<<blocks, 256, 0, stream>>>(codes, scales, rows, K, block, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

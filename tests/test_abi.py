@@ -73,5 +73,12 @@ def test_host_side_errors_before_launch(api):
     assert lib.moe_mxfp4_dequant(fake, fake, 4, 48, fake, None) == api.ESHAPE
     assert lib.moe_set_option(99, 1) == api.EINVAL
     assert lib.moe_set_option(api.OPT_WAIT_TIMEOUT_NS, 0) == api.EINVAL
+    # output layer: format, shape and workspace checks before any launch
+    assert lib.moe_lm_head(fake, 1, fake, None, 10, 256, 1, fake, fake, 1024, 0, None) == api.ESHAPE
+    assert lib.moe_lm_head(fake, 1, fake, None, 10, 264, 2, fake, fake, 1024, 0, None) == api.ESHAPE
+    assert lib.moe_lm_head(fake, 1, fake, None, 10, 256, 2, fake, fake, 1024, 0, None) == api.EINVAL
+    assert lib.moe_lm_head(fake, 17, fake, None, 10, 256, 0, fake, fake, 1024, 0, None) == api.EM
+    assert lib.moe_lm_head(fake, 1, fake, None, 10, 256, 0, fake, fake, 512, 0, None) == api.EWORKSPACE
+    assert lib.moe_fp8_quantize(fake, 4, 100, 32, fake, fake, None) == api.ESHAPE
     assert api.status_str(api.ETIMEOUT).startswith("device")
     assert api.last_launch_count() == 0
