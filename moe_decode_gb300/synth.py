@@ -202,6 +202,29 @@ def mxfp4_quantize(w: torch.Tensor):
 
 
 # ---------------------------------------------------------------------------
+# FP8 e4m3 encoding of synthetic weights
+
+FP8_BLOCK = 128
+
+
+def fp8_quantize(w: torch.Tensor, block: int = FP8_BLOCK):
+    """bf16/fp32 [..., K] -> (e4m3 codes uint8 [..., K], fp32 scales
+    [..., K / block]): scale = amax(block) / 448 in fp32 (1 for an all-zero
+    block), code = the e4m3 value nearest to w / scale (torch's float8
+    conversion: round to nearest even; the quotient never exceeds 448 by
+    more than a rounding error, and is clamped to +-448 first)."""
+    K = w.shape[-1]
+    assert K % block == 0
+    lead = w.shape[:-1]
+    v = w.to(torch.float32).reshape(-1, K // block, block)
+    amax = v.abs().amax(dim=-1)
+    sc = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    q = torch.clamp(v / sc.unsqueeze(-1), -448.0, 448.0)
+    codes = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.reshape(*lead, K), sc.reshape(*lead, K // block)
+
+
+# ---------------------------------------------------------------------------
 # activations
 
 def x_independent(shape: LayerShape, step: int, M: int, device="cpu") -> torch.Tensor:
@@ -234,7 +257,8 @@ def device_layer(shape: LayerShape, copy: int, wfmt: int = 0, device="cuda") -> 
 
     Keys: Wg, ws1, ws3, ws2 (bf16) and, for wfmt 0, w1, w3, w2 (bf16
     [E,I,H], [E,I,H], [E,H,I]); for wfmt 1, w1, w3, w2 as MXFP4 codes with
-    s1, s3, s2 scales (the bf16 draws quantised, expert block by block)."""
+    s1, s3, s2 scales; for wfmt 2, as FP8 e4m3 codes with fp32 scales per 128
+    elements (the bf16 draws quantised, expert block by block)."""
     d = {"Wg": router_weight(shape, copy, device)}
     d["ws1"], d["ws3"], d["ws2"] = shared_weights(shape, copy, device)
     E, H, I = shape.n_experts, shape.hidden, shape.inter
@@ -245,12 +269,16 @@ def device_layer(shape: LayerShape, copy: int, wfmt: int = 0, device="cuda") -> 
         return d
     blk = max(1, (1 << 24) // n)
     for name, tid, rows, K in (("w1", T_W1, I, H), ("w3", T_W3, I, H), ("w2", T_W2, H, I)):
-        codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
-        scales = torch.empty((E, rows, K // 32), dtype=torch.uint8, device=device)
+        if wfmt == 1:
+            codes = torch.empty((E, rows, K // 2), dtype=torch.uint8, device=device)
+            scales = torch.empty((E, rows, K // 32), dtype=torch.uint8, device=device)
+        else:
+            codes = torch.empty((E, rows, K), dtype=torch.uint8, device=device)
+            scales = torch.empty((E, rows, K // FP8_BLOCK), dtype=torch.float32, device=device)
         for e0 in range(0, E, blk):
             e1 = min(E, e0 + blk)
             w = normal_bf16(seed, tid, e0 * n, (e1 - e0) * n, WEIGHT_SIGMA, device).view(e1 - e0, rows, K)
-            codes[e0:e1], scales[e0:e1] = mxfp4_quantize(w)
+            codes[e0:e1], scales[e0:e1] = mxfp4_quantize(w) if wfmt == 1 else fp8_quantize(w)
         d[name] = codes
         d["s" + name[1]] = scales
     return d

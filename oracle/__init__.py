@@ -119,7 +119,8 @@ def expert(x_f32: np.ndarray, W1, W3, W2, wfmt: int = 0, S=(None, None, None),
     dt = np.uint16 if wfmt == 0 else np.uint8
     W1, W3, W2 = _c(W1, dt), _c(W3, dt), _c(W2, dt)
     I = W1.shape[0]
-    s1, s3, s2 = (None if s is None else _c(s, np.uint8) for s in S)
+    sdt = np.float32 if wfmt == 2 else np.uint8
+    s1, s3, s2 = (None if s is None else _c(s, sdt) for s in S)
     z = np.empty(H, dtype=np.float32)
     rc = _load().oracle_expert(_ptr(x_f32), H, I, wfmt, _ptr(W1), _ptr(s1), _ptr(W3),
                                _ptr(s3), _ptr(W2), _ptr(s2), int(acc_double), _ptr(z))
@@ -133,7 +134,8 @@ def ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict, E: int, I:
     """Expert FFN with given routing.
 
     experts maps expert id -> (W1, W3, W2) for bf16, or
-    (W1q, S1, W3q, S3, W2q, S2) for MXFP4; only the ids present in idx are
+    (W1q, S1, W3q, S3, W2q, S2) for MXFP4 (u8 scales) and FP8 (fp32 scales
+    per 128 elements); only the ids present in idx are
     needed. shared is (Ws1, Ws3, Ws2) bf16 or None. Returns y fp32 [M, H].
     """
     x = _c(x, np.uint16)
@@ -150,7 +152,8 @@ def ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict, E: int, I:
             vals = [_c(m, dt) for m in mats]
         else:
             names = ("W1", "S1", "W3", "S3", "W2", "S2")
-            vals = [_c(m, np.uint8) for m in mats]
+            sdt = np.float32 if wfmt == 2 else np.uint8
+            vals = [_c(m, np.uint8 if i % 2 == 0 else sdt) for i, m in enumerate(mats)]
         for n, v in zip(names, vals):
             keep.append(v)
             arr[n][int(e)] = v.ctypes.data

@@ -51,10 +51,17 @@ int oracle_mxfp4_decode(const uint8_t* codes, const uint8_t* scales,
     return 0;
 }
 
-/* One weight element as fp32: bf16 row-major, or MXFP4 codes + scales. */
+/* One weight element as fp32: bf16 row-major; MXFP4 codes + e8m0 scales
+ * (one per 32 elements of a row); or FP8 e4m3 codes + fp32 scales (one per
+ * 128 elements of a row, S then holds fp32 values). */
 static float weight_at(const void* W, const uint8_t* S, int wfmt, int K,
                        int64_t row, int col) {
     if (wfmt == 0) return oracle_bf16_to_f32(((const uint16_t*)W)[row * K + col]);
+    if (wfmt == 2) {
+        const uint8_t code = ((const uint8_t*)W)[row * K + col];
+        const float sc = ((const float*)S)[row * (K / 128) + col / 128];
+        return (float)(oracle_fp8_e4m3_value(code) * (double)sc);
+    }
     const uint8_t* q = (const uint8_t*)W;
     uint8_t byte = q[row * (K / 2) + col / 2];
     uint8_t code = (col & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15u);
@@ -153,7 +160,8 @@ int oracle_expert(const float* x, int H, int I, int wfmt,
                   int acc_double, float* z) {
     if (!x || !W1 || !W3 || !W2 || !z || H <= 0 || I <= 0) return -1;
     if (wfmt == 1 && (!s1 || !s3 || !s2 || H % 32 || I % 32)) return -1;
-    if (wfmt != 0 && wfmt != 1) return -1;
+    if (wfmt == 2 && (!s1 || !s3 || !s2 || H % 128 || I % 128)) return -1;
+    if (wfmt != 0 && wfmt != 1 && wfmt != 2) return -1;
     double* hd = (double*)malloc(sizeof(double) * (size_t)I);
     if (!hd) return -2;
     for (int i = 0; i < I; ++i) {
@@ -208,7 +216,7 @@ int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
                const uint16_t* Ws2, int acc_double, float* y) {
     if (!x || !y || M < 0 || H <= 0 || k < 0 || E <= 0 || I <= 0 || Is < 0) return -1;
     if (k > 0 && (!idx || !w || !W1 || !W3 || !W2)) return -1;
-    if (wfmt == 1 && k > 0 && (!S1 || !S3 || !S2)) return -1;
+    if (wfmt != 0 && k > 0 && (!S1 || !S3 || !S2)) return -1;
     if (Is > 0 && (!Ws1 || !Ws3 || !Ws2)) return -1;
     float* xt = (float*)malloc(sizeof(float) * (size_t)H);
     float* z = (float*)malloc(sizeof(float) * (size_t)H);
@@ -222,7 +230,7 @@ int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
             int e = idx[(int64_t)t * k + j];
             if (e < 0 || e >= E || !W1[e] || !W3[e] || !W2[e]) { rc = -3; break; }
             const uint8_t *a = NULL, *b = NULL, *d = NULL;
-            if (wfmt == 1) { a = S1[e]; b = S3[e]; d = S2[e]; }
+            if (wfmt != 0) { a = S1[e]; b = S3[e]; d = S2[e]; }
             rc = oracle_expert(xt, H, I, wfmt, W1[e], a, W3[e], b, W2[e], d, acc_double, z);
             if (rc) break;
             float wj = w[(int64_t)t * k + j];

@@ -79,6 +79,8 @@ int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
 
 /* One SwiGLU expert on one token: z = W2 (silu(W1 x) * (W3 x)).
  * wfmt 0: W1/W3/W2 are bf16, s1/s3/s2 ignored. wfmt 1: MXFP4 codes + scales.
+ * wfmt 2: FP8 e4m3 codes [rows, K] with fp32 scales [rows, K / 128] (the s
+ * pointers then point at fp32 values).
  * x is fp32 [H]; z is fp32 [H]. */
 int oracle_expert(const float* x, int H, int I, int wfmt,
                   const void* W1, const uint8_t* s1,

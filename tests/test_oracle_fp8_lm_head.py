@@ -100,3 +100,27 @@ def test_lm_head_linearity_permutation_and_precision(oracle):
     assert np.array_equal(oracle.lm_head(x, W[perm], V), base[:, perm])
     d = oracle.lm_head(x, W, V, acc_double=True).astype(np.float64)
     assert np.linalg.norm(base - d) / np.linalg.norm(d) < 1e-6
+
+
+def test_fp8_expert_equals_bf16_expert_on_exact_weights(oracle):
+    """An FP8 expert whose dequantised weights are exactly bf16 values
+    (e4m3 codes times power-of-two block scales) equals the bf16 expert on
+    those values bit for bit: pins the e4m3 decode and the per-128 scale
+    indexing of the expert path."""
+    rng = np.random.default_rng(5)
+    H, I = 256, 128
+    def make(rows, K):
+        codes = rng.integers(0, 256, (rows, K)).astype(np.uint8)
+        codes[(codes & 0x7f) == 0x7f] = 0x3c              # no NaN codes
+        sc = (2.0 ** rng.integers(-12, -4, (rows, K // 128))).astype(np.float32)
+        val = np.array([[oracle.fp8_e4m3_value(c) for c in row] for row in codes]) * np.repeat(sc, 128, axis=1)
+        bits = val.astype(np.float32).view(np.uint32)
+        assert np.all((bits & 0xFFFF) == 0)               # exactly bf16
+        return codes, sc, (bits >> 16).astype(np.uint16)
+    c1, s1, b1 = make(I, H)
+    c3, s3, b3 = make(I, H)
+    c2, s2, b2 = make(H, I)
+    x = oracle.bf16_to_f32(synth.to_u16(synth.normal_bf16(9, 9, 0, H, 1.0)))
+    z8 = oracle.expert(x, c1, c3, c2, wfmt=2, S=(s1, s3, s2))
+    zb = oracle.expert(x, b1, b3, b2, wfmt=0)
+    assert np.array_equal(z8, zb)

@@ -49,3 +49,18 @@ def test_overlap_recipe_is_linear_mix():
     c = np.corrcoef(x.numpy())
     off = c[~np.eye(10, dtype=bool)]
     assert abs(off.mean() - synth.RHO_OVERLAP_M10) < 0.05
+
+
+def test_fp8_input_quantiser_matches_the_oracle_definition():
+    """The generator's FP8 encoding of synthetic weights (torch float8
+    conversion) gives the oracle quantiser's codes and scales bit for bit,
+    including an all-zero block and values at the top of the range."""
+    import oracle
+    oracle.build()
+    w = synth.normal_bf16(71, 1, 0, 6 * 384, 0.02).view(6, 384).clone()
+    w[2, :128] = 0
+    w[4, 5] = 3.0
+    c, s = synth.fp8_quantize(w)
+    co, so = oracle.fp8_quantize(synth.to_u16(w), 128)
+    assert np.array_equal(c.numpy(), co)
+    assert np.array_equal(s.numpy().view(np.uint32), so.view(np.uint32))
