@@ -40,6 +40,8 @@ WORKLOADS = {
     "ling_m10": dict(M=10, wfmt=0, copies=4, gen="overlap"),
     "mxfp4_m1": dict(M=1, wfmt=1, copies=8, gen="independent"),
     "mxfp4_m6": dict(M=6, wfmt=1, copies=8, gen="independent"),
+    "fp8_m1": dict(M=1, wfmt=2, copies=6, gen="independent"),
+    "fp8_m6": dict(M=6, wfmt=2, copies=6, gen="independent"),
     # small case for detailed profiler captures: the Ling layer cut to 128
     # experts (1.5 GB per copy), still far above L2
     "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128),
@@ -64,7 +66,8 @@ def layer_shape(name: str):
 def describe(name: str) -> str:
     w = WORKLOADS[name]
     E = w.get("E", 512)
-    fmt = "bf16" if w["wfmt"] == 0 else "MXFP4 (e2m1 + e8m0/32) routed experts, bf16 router and shared expert"
+    fmt = {0: "bf16", 1: "MXFP4 (e2m1 + e8m0/32) routed experts, bf16 router and shared expert",
+           2: "FP8 (e4m3 + fp32 scale/128) routed experts, bf16 router and shared expert"}[w["wfmt"]]
     gen = ("tokens drawn independently" if w["gen"] == "independent"
            else "tokens with ~50% consecutive top-8 overlap")
     return (f"Ling-shape MoE layer H=2560 E={E} top-8 I=768 shared I=768, {fmt}, M={w['M']} ({gen}), "
@@ -231,8 +234,10 @@ class Workload:
         U = int(self.distinct[s % PERIOD])
         if self.wfmt == 0:
             expert = 3 * H * I * 2
-        else:
+        elif self.wfmt == 1:
             expert = 2 * (I * H // 2 + I * H // 32) + (H * I // 2 + H * I // 32)
+        else:
+            expert = 3 * (H * I + H * I // 128 * 4)
         shared = 3 * H * sh.shared_inter * 2
         return E * H * 2 + U * expert + shared + 2 * self.M * H * 2 + self.M * sh.top_k * 8
 
@@ -414,7 +419,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="ling_m1")
-    ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6",
+    ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,fp8_m1,fp8_m6,"
+                                      "lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6",
                     help="comma-separated extra workloads measured in the same run ('' for none)")
     ap.add_argument("--cpu-steps", type=int, default=0,
                     help="oracle steps timed for cpu_baseline (0: about 12 s of oracle work for the workload)")
@@ -500,7 +506,7 @@ def main():
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if w["wfmt"] == 0 else "mxfp4-weights/bf16-act",
+        "dtype": {0: "bf16", 1: "mxfp4-weights/bf16-act", 2: "fp8-e4m3-weights/bf16-act"}[w["wfmt"]],
         "data": "synthetic (seeded counter-hash generator; N(0,0.02)-like weights, N(0,1)-like tokens)",
         "config": {"workload": describe(args.workload), "M": w["M"], "hidden": 2560,
                    "n_experts": w.get("E", 512),
@@ -558,7 +564,7 @@ def run_reference(args, rank: int, world: int):
             if w["wfmt"] == 0:
                 experts[int(e)] = tuple(synth.to_u16(m) for m in mats)
             else:
-                q = [synth.mxfp4_quantize(m) for m in mats]
+                q = [synth.mxfp4_quantize(m) if w["wfmt"] == 1 else synth.fp8_quantize(m) for m in mats]
                 experts[int(e)] = (q[0][0].cpu().numpy(), q[0][1].cpu().numpy(), q[1][0].cpu().numpy(),
                                    q[1][1].cpu().numpy(), q[2][0].cpu().numpy(), q[2][1].cpu().numpy())
         return x, copies[c][0], experts, copies[c][1]

@@ -44,6 +44,12 @@
  *     [E, I, H/32]; w2 u8 [E, H, I/2], s2 u8 [E, H, I/32]. Codes are e2m1,
  *     element 2j in the low nibble of byte j; scales are e8m0 (2^(s-127)),
  *     one per 32 consecutive elements of a row.
+ *   FP8 routed experts (wfmt = 2): w1, w3 u8 [E, I, H], s1, s3 fp32
+ *     [E, I, H/128]; w2 u8 [E, H, I], s2 fp32 [E, H, I/128] (the s pointers
+ *     of moe_weights then point at fp32 values). Codes are OCP e4m3; a weight
+ *     is e4m3(code) * scale, one scale per 128 consecutive elements of a row
+ *     ("Chasing the Batch-1 Floor", "Where the time goes now": FP8 block-128
+ *     experts; a 128 x 128 tile scale repeats over its 128 rows).
  *   ws1, ws3 bf16 [Is, H]; ws2 bf16 [H, Is]   shared expert (always bf16)
  *   idx    int32 [M, k]  selected experts, by descending logit (ties: lower
  *                        index first)
@@ -103,19 +109,19 @@ extern "C" {
                                      entries. 0 (default) disables it. */
 
 typedef struct moe_shape {
-    int32_t hidden;       /* H: multiple of 256 (bf16) or 512 (MXFP4), <= 8192 */
+    int32_t hidden;       /* H: multiple of 256 (bf16) or 512 (MXFP4, FP8), <= 8192 */
     int32_t n_experts;    /* E: 1..1024 */
     int32_t top_k;        /* k: 1..min(16, E) */
-    int32_t inter;        /* I: multiple of 64, at most 4096 */
+    int32_t inter;        /* I: multiple of 64 (FP8: 128), at most 4096 */
     int32_t shared_inter; /* Is: 0 (no shared expert) or a multiple of 64, <= 4096 */
-    int32_t wfmt;         /* routed expert weights: 0 = bf16, 1 = MXFP4 */
+    int32_t wfmt;         /* routed expert weights: 0 = bf16, 1 = MXFP4, 2 = FP8 e4m3 */
 } moe_shape;
 
 typedef struct moe_weights {
     const void* w1;     /* routed gate projection  (device) */
     const void* w3;     /* routed up projection    (device) */
     const void* w2;     /* routed down projection  (device) */
-    const uint8_t* s1;  /* MXFP4 scales of w1, w3, w2; NULL for bf16 */
+    const uint8_t* s1;  /* MXFP4 (u8) or FP8 (fp32) scales of w1, w3, w2; NULL for bf16 */
     const uint8_t* s3;
     const uint8_t* s2;
     const void* ws1;    /* shared expert, bf16; NULL when Is == 0 */

@@ -106,7 +106,9 @@ def make_shape(hidden, n_experts, top_k, inter, shared_inter, wfmt=0) -> Shape:
 class ExpertWeights:
     """Device tensors of one layer's experts (layouts in include/moe_decode.h).
     bf16: w1, w3 [E,I,H], w2 [E,H,I]; MXFP4: w1, w3 u8 [E,I,H/2], s1, s3 u8
-    [E,I,H/32], w2 u8 [E,H,I/2], s2 u8 [E,H,I/32]. Shared expert bf16."""
+    [E,I,H/32], w2 u8 [E,H,I/2], s2 u8 [E,H,I/32]; FP8: w1, w3 u8 [E,I,H],
+    s1, s3 fp32 [E,I,H/128], w2 u8 [E,H,I], s2 fp32 [E,H,I/128]. Shared
+    expert bf16."""
     w1: torch.Tensor
     w3: torch.Tensor
     w2: torch.Tensor

@@ -91,11 +91,11 @@ int check_shape(const moe_shape* s, int M) {
     if (!s) return MOE_EINVAL;
     if (M < 1 || M > moe::kMaxM) return MOE_EM;
     const int H = s->hidden, E = s->n_experts, k = s->top_k, I = s->inter, Is = s->shared_inter;
-    if (s->wfmt != 0 && s->wfmt != 1) return MOE_ESHAPE;
-    if (H <= 0 || H % (s->wfmt == 1 ? 512 : 256) != 0 || H > 8192) return MOE_ESHAPE;
+    if (s->wfmt != 0 && s->wfmt != 1 && s->wfmt != 2) return MOE_ESHAPE;
+    if (H <= 0 || H % (s->wfmt == 0 ? 256 : 512) != 0 || H > 8192) return MOE_ESHAPE;
     if (E < 1 || E > moe::kMaxE) return MOE_ESHAPE;
     if (k < 1 || k > moe::kMaxK || k > E) return MOE_ESHAPE;
-    if (I <= 0 || I % 64 != 0 || I > 4096) return MOE_ESHAPE;
+    if (I <= 0 || I % (s->wfmt == 2 ? 128 : 64) != 0 || I > 4096) return MOE_ESHAPE;
     if (Is < 0 || Is % 64 != 0 || Is > 4096) return MOE_ESHAPE;
     return MOE_OK;
 }
@@ -170,7 +170,9 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
 
 int launch(const LayerParams& p, int wfmt, cudaStream_t st, bool pdl, DeviceInfo& dev) {
     bool coop = dev.coop;
-    cudaError_t err = wfmt == 1 ? moe::launch_layer_mxfp4(p, st, pdl, coop) : moe::launch_layer_bf16(p, st, pdl, coop);
+    cudaError_t err = wfmt == 1   ? moe::launch_layer_mxfp4(p, st, pdl, coop)
+                      : wfmt == 2 ? moe::launch_layer_fp8(p, st, pdl, coop)
+                                  : moe::launch_layer_bf16(p, st, pdl, coop);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return MOE_ECUDA;
@@ -181,14 +183,14 @@ int launch(const LayerParams& p, int wfmt, cudaStream_t st, bool pdl, DeviceInfo
 
 bool weights_ok(const moe_weights* W, const moe_shape* s) {
     if (!W || !W->w1 || !W->w3 || !W->w2) return false;
-    if (s->wfmt == 1 && (!W->s1 || !W->s3 || !W->s2)) return false;
+    if (s->wfmt != 0 && (!W->s1 || !W->s3 || !W->s2)) return false;
     if (s->shared_inter > 0 && (!W->ws1 || !W->ws3 || !W->ws2)) return false;
     return true;
 }
 
 bool weights_aligned(const moe_weights* W, const moe_shape* s) {
     bool ok = aligned16(W->w1) && aligned16(W->w3) && aligned16(W->w2);
-    if (s->wfmt == 1) ok = ok && aligned16(W->s1) && aligned16(W->s3) && aligned16(W->s2);
+    if (s->wfmt != 0) ok = ok && aligned16(W->s1) && aligned16(W->s3) && aligned16(W->s2);
     if (s->shared_inter > 0) ok = ok && aligned16(W->ws1) && aligned16(W->ws3) && aligned16(W->ws2);
     return ok;
 }

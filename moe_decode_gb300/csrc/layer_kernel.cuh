@@ -59,14 +59,17 @@ struct Chunk {
 // next() returns false at the end of each phase; begin(ph) starts a phase.
 template <int WFMT>
 __device__ __forceinline__ int gateup_cap(const LayerParams& p, bool routed) {
-    uint32_t pair = (WFMT == 1 && routed) ? (uint32_t)(2 * (p.H / 2 + p.H / 32)) : (uint32_t)(4 * p.H);
+    // a routed row pair: codes plus scales (MXFP4 and FP8 both carry H / 32
+    // scale bytes per row)
+    uint32_t pair = !routed || WFMT == 0 ? (uint32_t)(4 * p.H)
+                    : (uint32_t)(2 * ((WFMT == 1 ? p.H / 2 : p.H) + p.H / 32));
     return (int)(SB / pair);
 }
 
 template <int WFMT>
 __device__ __forceinline__ uint32_t down_rowbytes(const LayerParams& p, int slot) {
     if (slot < 0) return (uint32_t)p.Is * 2;
-    return WFMT == 1 ? (uint32_t)(p.I / 2 + p.I / 32) : (uint32_t)p.I * 2;
+    return WFMT == 0 ? (uint32_t)p.I * 2 : (uint32_t)((WFMT == 1 ? p.I / 2 : p.I) + p.I / 32);
 }
 
 template <int WFMT>
@@ -142,7 +145,7 @@ struct ChunkGen {
             }
             // chunk geometry of this (slot, pair group), computed once
             const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * 2;
-            const uint32_t reserve = (WFMT == 1 && ds >= 0) ? 32u : 0u;
+            const uint32_t reserve = (WFMT != 0 && ds >= 0) ? 32u : 0u;
             np = min(pg, npairs - q0);
             rcap = (int)((SB - (uint32_t)np * hrow - reserve) / down_rowbytes<WFMT>(p, ds));
             h = h0;
@@ -311,11 +314,12 @@ struct Producer {
                 bulk_g2s(dst, a, b, bar, pol_w);
                 bulk_g2s(dst + b, c, b, bar, pol_w);
             } else {
-                const uint32_t bc = (uint32_t)ch.n * (p.H / 2), bs = (uint32_t)ch.n * (p.H / 32);
+                constexpr int CD = WFMT == 1 ? 2 : 1;  // elements per code byte
+                const uint32_t bc = (uint32_t)ch.n * (p.H / CD), bs = (uint32_t)ch.n * (p.H / 32);
                 const size_t row = (size_t)plan->slot_e[ch.slot] * p.I + ch.r0;
                 mbar_arrive_expect_tx(bar, 2 * bc + 2 * bs);
-                bulk_g2s(dst, p.w1 + row * (p.H / 2), bc, bar, pol_w);
-                bulk_g2s(dst + bc, p.w3 + row * (p.H / 2), bc, bar, pol_w);
+                bulk_g2s(dst, p.w1 + row * (p.H / CD), bc, bar, pol_w);
+                bulk_g2s(dst + bc, p.w3 + row * (p.H / CD), bc, bar, pol_w);
                 bulk_g2s(dst + 2 * bc, p.s1 + row * (p.H / 32), bs, bar, pol_w);
                 bulk_g2s(dst + 2 * bc + bs, p.s3 + row * (p.H / 32), bs, bar, pol_w);
             }
@@ -336,12 +340,13 @@ struct Producer {
                     mbar_arrive_expect_tx(bar, hb + wb);
                     bulk_g2s(dst + hb, p.w2 + row * p.I * 2, wb, bar, pol_w);
                 } else {
-                    const uint32_t bc = (uint32_t)ch.n * (p.I / 2);
+                    constexpr int CD = WFMT == 1 ? 2 : 1;
+                    const uint32_t bc = (uint32_t)ch.n * (p.I / CD);
                     const size_t s0 = row * (p.I / 32), s1 = s0 + (size_t)ch.n * (p.I / 32);
                     const size_t w0 = s0 & ~(size_t)15, w1 = (s1 + 15) & ~(size_t)15;
                     const uint32_t bs = (uint32_t)(w1 - w0);
                     mbar_arrive_expect_tx(bar, hb + bc + bs);
-                    bulk_g2s(dst + hb, p.w2 + row * (p.I / 2), bc, bar, pol_w);
+                    bulk_g2s(dst + hb, p.w2 + row * (p.I / CD), bc, bar, pol_w);
                     bulk_g2s(dst + hb + bc, p.s2 + w0, bs, bar, pol_w);
                 }
             }
@@ -610,6 +615,85 @@ __device__ __forceinline__ void dot4_mxh(const uint8_t* const (&crow)[4], const 
     }
 }
 
+// ---- FP8 e4m3 with one fp32 scale per 128 elements of a row: codes
+// decoded to fp32 by the hardware conversion, products in fp32; each 16-code
+// vector's partial sum is scaled by its block's scale.
+
+// FP8 gate and up rows (codes c1, c3; scales s1, s3 per 128 elements)
+// against bf16 tokens; this lane takes 16-element vectors lane, lane + 32, ...
+template <int NT>
+__device__ __forceinline__ void dot2_fp8(const uint4* __restrict__ c1, const float* __restrict__ s1,
+                                         const uint4* __restrict__ c3, const float* __restrict__ s3,
+                                         const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nvec,
+                                         int lane, float (&g)[NT], float (&u)[NT]) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
+#pragma unroll 2
+    for (int v = lane; v < nvec; v += 32) {
+        float f1[16], f3[16];
+        unpack16_e4m3(c1[v], f1);
+        unpack16_e4m3(c3[v], f3);
+        const float sc1 = s1[v >> 3], sc3 = s3[v >> 3];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint4* xt = t == 0 ? x0 : x1;
+            float fa[8], fb[8];
+            unpack8(xt[2 * v], fa);
+            unpack8(xt[2 * v + 1], fb);
+            float pg0 = 0.f, pg1 = 0.f, pu0 = 0.f, pu1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                pg0 = fmaf(f1[e], fa[e], pg0);
+                pg1 = fmaf(f1[8 + e], fb[e], pg1);
+                pu0 = fmaf(f3[e], fa[e], pu0);
+                pu1 = fmaf(f3[8 + e], fb[e], pu1);
+            }
+            g[t] = fmaf(pg0 + pg1, sc1, g[t]);
+            u[t] = fmaf(pu0 + pu1, sc3, u[t]);
+        }
+    }
+}
+
+// Four FP8 down rows (codes crow[j], scales srow[j], bytes of fp32) against
+// NT bf16 activation vectors.
+template <int NT>
+__device__ __forceinline__ void dot4_fp8(const uint8_t* const (&crow)[4], const uint8_t* const (&srow)[4],
+                                         const uint4* __restrict__ h0, const uint4* __restrict__ h1, int nvec,
+                                         int lane, float (&acc)[4][NT]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[j][t] = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+        float fh[NT][16];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint4* ht = t == 0 ? h0 : h1;
+            float a8[8], b8[8];
+            unpack8(ht[2 * v], a8);
+            unpack8(ht[2 * v + 1], b8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) fh[t][e] = a8[e], fh[t][8 + e] = b8[e];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float fw[16];
+            unpack16_e4m3(reinterpret_cast<const uint4*>(crow[j])[v], fw);
+            const float sc = reinterpret_cast<const float*>(srow[j])[v >> 3];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float q0 = 0.f, q1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    q0 = fmaf(fw[e], fh[t][e], q0);
+                    q1 = fmaf(fw[8 + e], fh[t][8 + e], q1);
+                }
+                acc[j][t] = fmaf(q0 + q1, sc, acc[j][t]);
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // ------------------------------------------------------------ consumer
@@ -664,12 +748,16 @@ struct Consumer {
             const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
             dot2_bf16<NT, WFMT == 1>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
         } else {
-            const size_t cb = (size_t)p.H / 2, sbytes = (size_t)p.H / 32;
+            const size_t cb = (size_t)p.H / (WFMT == 1 ? 2 : 1), sbytes = (size_t)p.H / 32;
             const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
             const uint4* c3 = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
             const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
             const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
-            dot2_mxh<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
+            if (WFMT == 1)
+                dot2_mxh<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
+            else
+                dot2_fp8<NT>(c1, reinterpret_cast<const float*>(s1), c3, reinterpret_cast<const float*>(s3),
+                             xrow(t0tok), xrow(t1tok), p.H / 16, lane, g, u);
         }
     }
 
@@ -725,7 +813,7 @@ struct Consumer {
         const bool shared = ch.slot < 0;
         const int gbase = (shared ? 0 : p.M + plan->slot_p0[ch.slot]) + ch.p0;  // pair index of q0 = 0
         size_t sofs = 0;
-        if (WFMT == 1 && !shared) {
+        if (WFMT != 0 && !shared) {
             const size_t s0 = ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * (p.I / 32);
             sofs = s0 - (s0 & ~(size_t)15);
         }
@@ -793,11 +881,12 @@ struct Consumer {
                 }
                 continue;
             }
-            // MXFP4 routed rows, four at a time (rows past the part's end
-            // repeat its last row; their results are dropped)
+            // MXFP4 / FP8 routed rows, four at a time (rows past the part's
+            // end repeat its last row; their results are dropped)
+            constexpr int CD = WFMT == 1 ? 2 : 1;
             const size_t hbytes = (size_t)ch.np * p.I * 2;
             const uint8_t* codes = st + hbytes;
-            const uint8_t* scls = st + hbytes + (size_t)ch.n * (p.I / 2) + sofs;
+            const uint8_t* scls = st + hbytes + (size_t)ch.n * (p.I / CD) + sofs;
             const int nblk = p.I / 32;
             for (int r = ra; r < rb; r += 4) {
                 const int nrow = min(4, rb - r);
@@ -806,7 +895,7 @@ struct Consumer {
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const int j = r - ch.r0 + min(jj, nrow - 1);
-                    crow[jj] = codes + (size_t)j * (p.I / 2);
+                    crow[jj] = codes + (size_t)j * (p.I / CD);
                     srow[jj] = scls + (size_t)j * nblk;
                 }
                 float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
@@ -814,7 +903,10 @@ struct Consumer {
                 for (; q0 + 2 <= ch.np; q0 += 2) {
                     float acc[4][2];
                     const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
-                    dot4_mxh<2>(crow, srow, ha, ha + p.I / 8, nblk, lane, acc);
+                    if (WFMT == 1)
+                        dot4_mxh<2>(crow, srow, ha, ha + p.I / 8, nblk, lane, acc);
+                    else
+                        dot4_fp8<2>(crow, srow, ha, ha + p.I / 8, p.I / 16, lane, acc);
 #pragma unroll
                     for (int o = 16; o; o >>= 1)
 #pragma unroll
@@ -831,7 +923,10 @@ struct Consumer {
                 if (q0 < ch.np) {
                     float acc[4][1];
                     const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
-                    dot4_mxh<1>(crow, srow, ha, ha, nblk, lane, acc);
+                    if (WFMT == 1)
+                        dot4_mxh<1>(crow, srow, ha, ha, nblk, lane, acc);
+                    else
+                        dot4_fp8<1>(crow, srow, ha, ha, p.I / 16, lane, acc);
 #pragma unroll
                     for (int o = 16; o; o >>= 1)
 #pragma unroll
@@ -1062,7 +1157,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
-            if (WFMT == 0) {
+            if (WFMT != 1) {
                 for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
             } else {
                 // MXFP4 layers hold the tokens in f16 times 2^s_t, s_t chosen

@@ -8,7 +8,7 @@ namespace moe {
 // Consumer warps per CTA for each routed-weight format; one producer warp
 // comes on top. The total (12 warps) spreads evenly over the SM's four
 // schedulers and keeps the per-thread register budget at 168.
-constexpr int consumer_warps(int wfmt) { return wfmt == 0 ? 11 : 11; }
+constexpr int consumer_warps(int) { return 11; }
 constexpr int block_threads(int wfmt) { return (consumer_warps(wfmt) + 1) * 32; }
 constexpr uint32_t kStageBytes = 32768;               // one ring stage
 constexpr int kMaxStages = 6;

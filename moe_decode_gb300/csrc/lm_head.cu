@@ -50,30 +50,6 @@ __device__ __forceinline__ float lm_warp_sum(float v) {
     return v;
 }
 
-// Two e4m3 codes (a 16-bit half-word; element 2j in the low byte) to an f16
-// pair with the hardware conversion (every e4m3 value is exact in f16).
-__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(v));
-}
-
-// Sixteen e4m3 codes (one uint4) as fp32.
-__device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t lo, hi;
-        e4m3x4_to_f16x2(w[k], lo, hi);
-        const float2 a = f16x2_to_f32(lo), b = f16x2_to_f32(hi);
-        f[4 * k + 0] = a.x;
-        f[4 * k + 1] = a.y;
-        f[4 * k + 2] = b.x;
-        f[4 * k + 3] = b.y;
-    }
-}
-
 // acc[t] = row . x_t over H elements; this lane takes 16-byte weight vectors
 // lane, lane + 32, ... (bf16: 8 elements, e4m3: 16 elements per vector).
 template <int WT, int NT>

@@ -172,6 +172,32 @@ __device__ __forceinline__ int f16_range_shift(float mx) {
     return max(-100, min(100, 7 - e));
 }
 
+// ---------------------------------------------------------------- FP8 e4m3
+// Four e4m3 codes (one 32-bit word; element j in byte j) to two f16 pairs
+// with the hardware conversion: lo holds elements 0, 1 and hi elements 2, 3
+// (every e4m3 value is exact in f16).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(v));
+}
+
+// Sixteen e4m3 codes (one uint4) as fp32.
+__device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t lo, hi;
+        e4m3x4_to_f16x2(w[k], lo, hi);
+        const float2 a = f16x2_to_f32(lo), b = f16x2_to_f32(hi);
+        f[4 * k + 0] = a.x;
+        f[4 * k + 1] = a.y;
+        f[4 * k + 2] = b.x;
+        f[4 * k + 3] = b.y;
+    }
+}
+
 // 2^(s-127) for an e8m0 byte s (s = 0 is the subnormal 2^-127; s = 255 NaN).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
     if (s == 255u) return __uint_as_float(0x7fc00000u);

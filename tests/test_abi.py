@@ -51,7 +51,9 @@ def test_workspace_bytes_and_shape_checks(api):
                 api.make_shape(2560, 4, 8, 768, 768),     # k > E
                 api.make_shape(2560, 2048, 8, 768, 768),  # E > 1024
                 api.make_shape(2560, 512, 8, 700, 768),   # I % 64
-                api.make_shape(2560, 512, 8, 768, 768, 2),
+                api.make_shape(2560, 512, 8, 768, 768, 3),  # no such format
+                api.make_shape(2560, 512, 8, 704, 768, 2),  # FP8 needs I % 128
+                api.make_shape(2816, 512, 8, 768, 768, 2),  # FP8 needs H % 512
                 api.make_shape(256, 16, 2, 64, 64, 1)):   # MXFP4 needs H % 512
         assert api.workspace_bytes(bad, 1) == 0
 

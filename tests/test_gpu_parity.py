@@ -156,6 +156,50 @@ def test_ling_mxfp4(ling_mxfp4, M):
     pu.compare_layer(synth.LING, ling_mxfp4, x, 1)
 
 
+# ------------------------------------------------------------------ FP8
+
+TINY_FP8 = synth.LayerShape(hidden=512, n_experts=16, top_k=2, inter=128, shared_inter=64)
+
+
+@pytest.fixture(scope="module")
+def ling_fp8(api):
+    d = synth.device_layer(synth.LING, 0, wfmt=2)
+    yield d
+    del d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M", [1, 6])
+def test_ling_fp8(ling_fp8, M):
+    x = synth.x_independent(synth.LING, 30 + M, M, device="cuda")
+    pu.compare_layer(synth.LING, ling_fp8, x, 2)
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 16])
+def test_tiny_fp8_m_sweep(api, M):
+    layer = synth.device_layer(TINY_FP8, 1, wfmt=2)
+    x = synth.x_independent(TINY_FP8, 40 + M, M, device="cuda")
+    pu.compare_layer(TINY_FP8, layer, x, 2)
+
+
+@pytest.mark.parametrize("G", [1, 7, 19])
+def test_tiny_fp8_uneven_grids(api, G):
+    layer = synth.device_layer(TINY_FP8, 2, wfmt=2)
+    x = synth.x_independent(TINY_FP8, 50 + G, 3, device="cuda")
+    api.set_option(api.OPT_GRID_CTAS, G)
+    try:
+        pu.compare_layer(TINY_FP8, layer, x, 2)
+    finally:
+        api.set_option(api.OPT_GRID_CTAS, 0)
+
+
+def test_fp8_no_shared_expert(api):
+    sh = synth.LayerShape(hidden=512, n_experts=16, top_k=3, inter=256, shared_inter=0)
+    layer = synth.device_layer(sh, 3, wfmt=2)
+    x = synth.x_independent(sh, 60, 4, device="cuda")
+    pu.compare_layer(sh, layer, x, 2)
+
+
 def test_mxfp4_dequant_bit_exact(api):
     # every (code, scale) pair: row s holds codes 0..15 twice under scale s
     lo = np.arange(0, 16, 2, dtype=np.uint8)
