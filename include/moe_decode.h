@@ -29,10 +29,11 @@
  *    moe_ffn, a bounded wait that ran out) do not fault: they are written to
  *    a status word inside the workspace; read it with moe_read_status.
  *  - A workspace (`ws`, `ws_bytes` >= moe_workspace_bytes(shape, M)) holds
- *    the router logits, the SwiGLU activations and the grid-barrier counters.
- *    Zero it once with moe_workspace_init before its first use; every call
- *    leaves the counters zeroed again. Calls that share a workspace must be
- *    ordered on one stream (or otherwise serialised).
+ *    the router logits (each tagged with its call), the SwiGLU activations,
+ *    a call counter and the grid-barrier counters. Zero it once with
+ *    moe_workspace_init before its first use; every call leaves it ready for
+ *    the next. Calls that share a workspace must be ordered on one stream
+ *    (or otherwise serialised).
  *
  * Layouts (row-major; nn.Linear [out, in], contiguous along the reduction
  * dimension):
@@ -89,12 +90,12 @@ extern "C" {
 #define MOE_F_NO_PDL 1u                /* launch without programmatic
                                           dependent launch */
 #define MOE_F_RESET_SCRATCH 2u          /* moe_decode_layer_static_scratch
-                                          only: zero the static scratch's
-                                          control words before the launch */
-#define MOE_F_DEBUG_FORCE_TIMEOUT 256u /* test hook: the first grid barrier
-                                          waits for one CTA more than exists,
-                                          so it runs out and reports
-                                          MOE_ETIMEOUT */
+                                          only: zero the static scratch
+                                          before the launch */
+#define MOE_F_DEBUG_FORCE_TIMEOUT 256u /* test hook: the routing step waits
+                                          for router logits of a call that
+                                          never comes, so the wait runs out
+                                          and reports MOE_ETIMEOUT */
 
 /* options of moe_set_option */
 #define MOE_OPT_GRID_CTAS 1       /* CTAs of the persistent grid; 0 = one per
@@ -133,8 +134,8 @@ typedef struct moe_weights {
  * the library rejects. */
 size_t moe_workspace_bytes(const moe_shape* shape, int M);
 
-/* Zeroes the workspace (device, ws_bytes) on `stream`; needed once before
- * the first call and after a call reported MOE_ETIMEOUT. */
+/* Zeroes the whole workspace (device, ws_bytes) on `stream`; needed once
+ * before the first call and after a call reported MOE_ETIMEOUT. */
 int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Router alone: logits = x Wg^T in fp32, softmax, top-k, renormalised
@@ -174,7 +175,7 @@ int moe_decode_layer(const void* x, int M, const void* Wg,
  * workspace is a fixed array of MOE_STATIC_SCRATCH_BYTES in the library's
  * own device memory (one per device, created when the module loads). The
  * call allocates and frees nothing; its first call on a device looks the
- * array up and zeroes its control words on `stream`.
+ * array up and zeroes it on `stream`.
  *  - Returns MOE_ESCRATCH, before touching the device, when the shape and M
  *    need more than MOE_STATIC_SCRATCH_BYTES of workspace
  *    (moe_workspace_bytes > MOE_STATIC_SCRATCH_BYTES).

@@ -61,7 +61,7 @@ int device_info(DeviceInfo* out) {
 void* g_scratch_ptr[kMaxDevices];
 
 // Device address of this device's static scratch; the first call on a device
-// looks it up and zeroes its control words on `st`.
+// looks it up and zeroes it on `st`.
 int static_scratch(void** out, cudaStream_t st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -72,7 +72,7 @@ int static_scratch(void** out, cudaStream_t st) {
     if (!g_scratch_ptr[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess ||
-            cudaMemsetAsync(ptr, 0, moe::kCtlBytes, st) != cudaSuccess) {
+            cudaMemsetAsync(ptr, 0, MOE_STATIC_SCRATCH_BYTES, st) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ECUDA;
         }
@@ -108,7 +108,7 @@ WsLayout ws_layout(const moe_shape* s, int M) {
     WsLayout w;
     size_t off = moe::kCtlBytes;
     w.logits = off;
-    off = align_up(off + (size_t)M * s->n_experts * 4, 256);
+    off = align_up(off + (size_t)M * ((s->n_experts + 1) & ~1) * 8, 256);
     w.hs = off;
     off = align_up(off + (size_t)M * s->shared_inter * 2, 256);
     w.hr = off;
@@ -140,7 +140,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.trace = g_opt.trace;
     uint8_t* base = static_cast<uint8_t*>(ws);
     p.ctrl = reinterpret_cast<unsigned*>(base);
-    p.logits = reinterpret_cast<float*>(base + wl.logits);
+    p.logits = reinterpret_cast<unsigned long long*>(base + wl.logits);
+    p.Es = (s->n_experts + 1) & ~1;
     p.hs = reinterpret_cast<uint16_t*>(base + wl.hs);
     p.hr = reinterpret_cast<uint16_t*>(base + wl.hr);
 
@@ -219,7 +220,7 @@ size_t moe_workspace_bytes(const moe_shape* shape, int M) {
 int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws) return MOE_EINVAL;
     if (ws_bytes < moe::kCtlBytes) return MOE_EWORKSPACE;
-    if (cudaMemsetAsync(ws, 0, moe::kCtlBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    if (cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ECUDA;
     }
@@ -300,7 +301,7 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     void* ws = nullptr;
     rc = static_scratch(&ws, st);
     if (rc) return rc;
-    if ((flags & MOE_F_RESET_SCRATCH) && cudaMemsetAsync(ws, 0, moe::kCtlBytes, st) != cudaSuccess) {
+    if ((flags & MOE_F_RESET_SCRATCH) && cudaMemsetAsync(ws, 0, MOE_STATIC_SCRATCH_BYTES, st) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ECUDA;
     }

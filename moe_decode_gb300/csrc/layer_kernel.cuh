@@ -3,14 +3,14 @@
 // One CTA per SM. Each CTA runs one producer warp, whose elected lane streams
 // weight tiles from HBM into a ring of shared-memory stages with bulk (TMA)
 // copies completing on mbarriers, and consumer warps (consumer_warps(WFMT))
-// that compute from the ring. The layer runs in three phases separated by two
-// bounded grid barriers:
+// that compute from the ring. The layer runs in three phases, separated by a
+// bounded wait on tagged data (the logits) and a bounded grid barrier:
 //
 //   phase 0  router gate matvec: CTA c owns router rows [cE/G, (c+1)E/G);
-//            logits go to the workspace.              -> grid barrier 1
-//            Every CTA then computes softmax / top-k / renormalisation for
-//            all M tokens and builds the expert plan (distinct experts and
-//            their token lists) in shared memory.
+//            logits go to the workspace, each with this call's tag.
+//            Every CTA then waits for all tagged logits, computes softmax /
+//            top-k / renormalisation for all M tokens and builds the expert
+//            plan (distinct experts and their token lists) in shared memory.
 //   phase 1  gate/up + SwiGLU: the intermediate rows of the shared expert and
 //            of every touched routed expert are split evenly over the CTAs;
 //            h = silu(W1 x) * (W3 x) goes to the workspace in bf16.
@@ -735,7 +735,11 @@ struct Consumer {
                 dot_bf16<1, 32, WFMT == 1>(row, xt, xt, nvec, lane, acc);
                 acc[0] = warp_sum(acc[0]);
                 if (WFMT == 1) acc[0] *= plan->x_inv[t];
-                if (lane == 0) p.logits[(size_t)t * p.E + ch.r0 + j] = acc[0];
+                // the logit and this call's tag in one 64-bit word: readers
+                // need no barrier, they wait for the tag
+                if (lane == 0)
+                    st_relaxed_u64(p.logits + (size_t)t * p.Es + ch.r0 + j,
+                                   ((unsigned long long)plan->tag << 32) | __float_as_uint(acc[0]));
             }
         }
     }
@@ -966,29 +970,57 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
 }
 
 // Softmax, top-k (descending logit, ties to the lower expert index) and
-// renormalisation for one token, by one warp. Lane l holds the logits of
-// experts l, l + 32, ... (EPL of them) and keeps its own best entry; each of
-// the k rounds takes the warp maximum with one hardware reduction, the lowest
-// expert index among the lanes holding it with a second, and the winning lane
-// rescans its entries. The code stays small on purpose: it runs once per
-// launch, so its instructions are fetched cold. The full softmax denominator
-// cancels in the renormalisation, so
+// renormalisation for one token, by one warp. The logits come from every CTA
+// as 64-bit words (logit, tag): the warp reads them with relaxed loads until
+// every tag is this call's (a bounded wait; no grid barrier). Lane l holds
+// the logits of experts 64j + 2l and 64j + 2l + 1 (EPL of them) and keeps its
+// own best entry; each of the k rounds takes the warp maximum with one
+// hardware reduction, the lowest expert index among the lanes holding it with
+// a second, and the winning lane rescans its entries. The code stays small on
+// purpose: it runs once per launch, so its instructions are fetched cold. The
+// full softmax denominator cancels in the renormalisation, so
 // w_j = exp(l_j - max) / sum over the selected of exp(l - max).
+// Returns false when the wait ran out (the CTA is then aborted).
 template <int EPL>
-__device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int E, const int k, int lane,
+__device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lrow, const int E, const int k,
+                                       int lane, uint32_t tag, const LayerParams& p, Plan* plan,
                                        int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
     uint32_t key[EPL];
+    uint64_t t0 = 0;
+    for (int spin = 0;; ++spin) {
+        bool ok = true;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = e < E ? f32_key(__ldcg(lrow + e)) : 0u;
+        for (int j = 0; j < EPL / 2; ++j) {
+            const int e = 64 * j + 2 * lane;
+            key[2 * j] = key[2 * j + 1] = 0u;
+            if (e < E) {
+                unsigned long long a, b;
+                ld_relaxed_v2u64(lrow + e, a, b);
+                ok = ok && (uint32_t)(a >> 32) == tag;
+                key[2 * j] = f32_key(__uint_as_float((uint32_t)a));
+                if (e + 1 < E) {
+                    ok = ok && (uint32_t)(b >> 32) == tag;
+                    key[2 * j + 1] = f32_key(__uint_as_float((uint32_t)b));
+                }
+            }
+        }
+        if (__all_sync(0xffffffffu, ok)) break;
+        if (spin == 0) t0 = global_timer_ns();
+        if (aborted(plan)) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            if (lane == 0) set_abort(p, plan, -101 /* MOE_ETIMEOUT */);
+            __syncwarp();
+            return false;
+        }
+        __nanosleep(64);
     }
+    auto idx_of = [lane](int j) { return (uint32_t)(64 * (j >> 1) + 2 * lane + (j & 1)); };
     uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
         if (key[j] > bk) {
             bk = key[j];
-            bi = (uint32_t)(lane + 32 * j);
+            bi = idx_of(j);
         }
     float mx = 0.f, mine = 0.f;
     for (int jj = 0; jj < k; ++jj) {
@@ -1003,10 +1035,10 @@ __device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int
             bi = 0xffffffffu;
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
-                if ((uint32_t)(lane + 32 * j) == we) key[j] = 0u;
+                if (idx_of(j) == we) key[j] = 0u;
                 if (key[j] > bk) {
                     bk = key[j];
-                    bi = (uint32_t)(lane + 32 * j);
+                    bi = idx_of(j);
                 }
             }
         }
@@ -1016,16 +1048,20 @@ __device__ __noinline__ void topk_warp(const float* __restrict__ lrow, const int
 #pragma unroll
     for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (lane < k) sel_w[lane] = ex / den;
+    return true;
 }
 
-static __device__ __forceinline__ void topk_tokens(const float* __restrict__ logits, const int M, const int E,
-                                                   const int k, Plan* plan, int warp, int lane, int nwarps) {
-    for (int t = warp; t < M; t += nwarps) {
-        const float* lrow = logits + (size_t)t * E;
-        if (E <= 512)
-            topk_warp<16>(lrow, E, k, lane, plan->sel_e + t * k, plan->sel_w + t * k);
-        else
-            topk_warp<32>(lrow, E, k, lane, plan->sel_e + t * k, plan->sel_w + t * k);
+static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* plan, int warp, int lane,
+                                                   int nwarps) {
+    // the debug hook waits for a tag that never comes
+    const uint32_t tag = plan->tag + (p.force_timeout ? 1u : 0u);
+    for (int t = warp; t < p.M; t += nwarps) {
+        const unsigned long long* lrow = p.logits + (size_t)t * p.Es;
+        const bool ok = p.E <= 512 ? topk_warp<16>(lrow, p.E, p.k, lane, tag, p, plan, plan->sel_e + t * p.k,
+                                                   plan->sel_w + t * p.k)
+                                   : topk_warp<32>(lrow, p.E, p.k, lane, tag, p, plan, plan->sel_e + t * p.k,
+                                                   plan->sel_w + t * p.k);
+        if (!ok) return;
     }
 }
 
@@ -1153,6 +1189,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
         Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0, 0};
         pdl_wait();
+        if (tid == 0) plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
@@ -1200,16 +1237,10 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         bool ok = true;
         if (has_route) {
             for (gen.begin(0, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
-            named_bar_sync(1, NCT);  // this CTA's logits are stored
             if (tid == 0) trace_mark(p, 2);
-            if (tid == 0 && !aborted(plan)) {
-                __threadfence();
-                atomicAdd(p.ctrl + kCtlBar1, 1u);
-                grid_wait(p.ctrl + kCtlBar1, (unsigned)p.G + (p.force_timeout ? 1u : 0u), p, plan);
-            }
-            named_bar_sync(1, NCT);
+            // no grid barrier: each token's warp waits for the tagged logits
+            if (!aborted(plan)) topk_tokens(p, plan, warp, lane, NCW);
             if (tid == 0) trace_mark(p, 4);
-            if (!aborted(plan)) topk_tokens(p.logits, p.M, p.E, p.k, plan, warp, lane, NCW);
             named_bar_sync(1, NCT);
             if (cta == 0 && !aborted(plan)) {
                 for (int i = tid; i < p.M * p.k; i += NCT) {
@@ -1259,8 +1290,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         __threadfence();
         const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
         if (old == (unsigned)p.G - 1u) {
-            atomicExch(p.ctrl + kCtlBar1, 0u);
             atomicExch(p.ctrl + kCtlBar2, 0u);
+            atomicAdd(p.ctrl + kCtlEpoch, 1u);  // the next call's tag
             atomicExch(p.ctrl + kCtlExit, 0u);
         }
     }

@@ -17,9 +17,10 @@ constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
 
-// workspace control block (uint32 words; counters 128 bytes apart)
+// workspace control block (uint32 words, 128 bytes apart): status, launch
+// epoch (advanced by the last CTA of every call), grid barrier, exit counter
 constexpr int kCtlStatus = 0;
-constexpr int kCtlBar1 = 32;
+constexpr int kCtlEpoch = 32;
 constexpr int kCtlBar2 = 64;
 constexpr int kCtlExit = 96;
 constexpr uint32_t kCtlBytes = 1024;
@@ -44,7 +45,10 @@ struct LayerParams {
     float* w_out;
     uint16_t* y;           // [M, H] bf16
     unsigned* ctrl;        // workspace control block
-    float* logits;         // [M, E]
+    // router logits [M, Es]: 64-bit words, the fp32 logit in the low half and
+    // the call's tag in the high half (Es = E rounded up to even)
+    unsigned long long* logits;
+    int Es;
     uint16_t* hs;          // shared-expert activations [M, Is] bf16
     uint16_t* hr;          // routed activations [M*k, I] bf16, grouped by expert
     int M, H, E, k, I, Is;
@@ -72,6 +76,7 @@ struct Plan {
                                     // 2^s_t; x_inv[t] = 2^-s_t
     int32_t nslot;
     int32_t npairs;
+    uint32_t tag;                   // this call's tag: 1 + epoch mod (2^32 - 1)
     int32_t abort;
     int32_t pad;
     // Activation copies of down chunks issued before grid barrier 2

@@ -119,6 +119,16 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// Relaxed GPU-scope 64-bit store and paired 64-bit load. Each aligned
+// 64-bit word is single-copy atomic: a reader sees it whole, old or new.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void ld_relaxed_v2u64(const unsigned long long* p, unsigned long long& a,
+                                                 unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 // ---------------------------------------------------------------- bf16
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
