@@ -52,6 +52,7 @@ def _load():
         lib.oracle_mxfp4_value.restype = ctypes.c_float
         lib.oracle_mxfp4_decode.argtypes = [P, P, i64, i32, P]
         lib.oracle_route.argtypes = [P, i32, i32, P, i32, i32, i32, P, P, P]
+        lib.oracle_route_ex.argtypes = [P, i32, i32, P, i32, i32, i32, P, ctypes.c_float, i32, P, P, P]
         lib.oracle_fp8_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.oracle_fp8_e4m3_value.restype = ctypes.c_double
         lib.oracle_fp8_e4m3_encode.argtypes = [ctypes.c_float]
@@ -108,6 +109,25 @@ def route(x: np.ndarray, Wg: np.ndarray, k: int, acc_double: bool = False):
                               _ptr(logits), _ptr(idx), _ptr(w))
     if rc:
         raise ValueError(f"oracle_route rc={rc}")
+    return idx, w, logits
+
+
+def route_ex(x: np.ndarray, Wg: np.ndarray, k: int, scoring: int = 0, bias=None, routed_scale: float = 1.0,
+             acc_double: bool = False):
+    """Router with scoring 0 (softmax) or 1 (sigmoid), an optional selection
+    bias [E] and a routed scaling factor. Returns (idx, w, logits)."""
+    x = _c(x, np.uint16)
+    Wg = _c(Wg, np.uint16)
+    M, H = x.shape
+    E = Wg.shape[0]
+    b = None if bias is None else _c(bias, np.float32)
+    idx = np.empty((M, k), dtype=np.int32)
+    w = np.empty((M, k), dtype=np.float32)
+    logits = np.empty((M, E), dtype=np.float32)
+    rc = _load().oracle_route_ex(_ptr(x), M, H, _ptr(Wg), E, k, scoring, _ptr(b), routed_scale, int(acc_double),
+                                 _ptr(logits), _ptr(idx), _ptr(w))
+    if rc:
+        raise ValueError(f"oracle_route_ex rc={rc}")
     return idx, w, logits
 
 

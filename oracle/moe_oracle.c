@@ -75,14 +75,20 @@ static float weight_at(const void* W, const uint8_t* S, int wfmt, int K,
  * renormalisation of the k selected probabilities is the plain reading of
  * "routes each token to eight of 512 routed experts" ("3 ways to boost MoE
  * inference", section "Model and baseline configuration"). */
-int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
-                 int k, int acc_double, float* logits, int32_t* idx, float* w) {
+int oracle_route_ex(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
+                    int k, int scoring, const float* bias, float routed_scale,
+                    int acc_double, float* logits, int32_t* idx, float* w) {
     if (!x || !Wg || !idx || !w || M < 0 || H <= 0 || E <= 0 || k <= 0 || k > E)
         return -1;
+    if (scoring != 0 && scoring != 1) return -1;
+    const double scale = routed_scale > 0.0f ? (double)routed_scale : 1.0;
+    /* softmax without a bias ranks the logits themselves (the same order) */
+    const int by_logit = scoring == 0 && !bias;
     double* l = (double*)malloc(sizeof(double) * (size_t)E);
     double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* c = (double*)malloc(sizeof(double) * (size_t)E);
     unsigned char* taken = (unsigned char*)malloc((size_t)E);
-    if (!l || !p || !taken) { free(l); free(p); free(taken); return -2; }
+    if (!l || !p || !c || !taken) { free(l); free(p); free(c); free(taken); return -2; }
     for (int t = 0; t < M; ++t) {
         const uint16_t* xt = x + (int64_t)t * H;
         /* step 1: logits, accumulated in index order */
@@ -103,49 +109,66 @@ int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
             }
             if (logits) logits[(int64_t)t * E + e] = (float)l[e];
         }
-        /* step 2: softmax over all E (max-subtracted) */
-        double mx = l[0];
-        for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
-        if (acc_double) {
-            double den = 0.0;
-            for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); den += p[e]; }
-            for (int e = 0; e < E; ++e) p[e] /= den;
-        } else {
-            float den = 0.0f;
-            for (int e = 0; e < E; ++e) {
-                float pe = expf((float)l[e] - (float)mx);
-                p[e] = (double)pe;
-                den = den + pe;
+        /* step 2: scores: softmax over all E (max-subtracted), or the
+         * logistic function of each logit */
+        if (scoring == 0) {
+            double mx = l[0];
+            for (int e = 1; e < E; ++e) if (l[e] > mx) mx = l[e];
+            if (acc_double) {
+                double den = 0.0;
+                for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); den += p[e]; }
+                for (int e = 0; e < E; ++e) p[e] /= den;
+            } else {
+                float den = 0.0f;
+                for (int e = 0; e < E; ++e) {
+                    float pe = expf((float)l[e] - (float)mx);
+                    p[e] = (double)pe;
+                    den = den + pe;
+                }
+                for (int e = 0; e < E; ++e) p[e] = (double)((float)p[e] / den);
             }
-            for (int e = 0; e < E; ++e) p[e] = (double)((float)p[e] / den);
+        } else {
+            for (int e = 0; e < E; ++e)
+                p[e] = acc_double ? 1.0 / (1.0 + exp(-l[e]))
+                                  : (double)(1.0f / (1.0f + expf(-(float)l[e])));
         }
-        /* step 3: the k largest logits; ties go to the lower index. Softmax
-         * is monotone, so ranking logits ranks probabilities. */
+        /* step 3: the k largest selection keys (logit; or score plus the
+         * expert's bias), ties to the lower index */
+        for (int e = 0; e < E; ++e) {
+            const double b = bias ? (double)bias[e] : 0.0;
+            c[e] = by_logit ? l[e] : acc_double ? p[e] + b : (double)((float)p[e] + (float)b);
+        }
         memset(taken, 0, (size_t)E);
         for (int j = 0; j < k; ++j) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
                 if (taken[e]) continue;
-                if (best < 0 || l[e] > l[best]) best = e;
+                if (best < 0 || c[e] > c[best]) best = e;
             }
             taken[best] = 1;
             idx[(int64_t)t * k + j] = best;
         }
-        /* step 4: renormalise the selected probabilities */
+        /* step 4: the selected (unbiased) scores renormalised to sum to one,
+         * times the routed scaling factor */
         if (acc_double) {
             double s = 0.0;
             for (int j = 0; j < k; ++j) s += p[idx[(int64_t)t * k + j]];
             for (int j = 0; j < k; ++j)
-                w[(int64_t)t * k + j] = (float)(p[idx[(int64_t)t * k + j]] / s);
+                w[(int64_t)t * k + j] = (float)(p[idx[(int64_t)t * k + j]] / s * scale);
         } else {
             float s = 0.0f;
             for (int j = 0; j < k; ++j) s = s + (float)p[idx[(int64_t)t * k + j]];
             for (int j = 0; j < k; ++j)
-                w[(int64_t)t * k + j] = (float)p[idx[(int64_t)t * k + j]] / s;
+                w[(int64_t)t * k + j] = (float)p[idx[(int64_t)t * k + j]] / s * (float)scale;
         }
     }
-    free(l); free(p); free(taken);
+    free(l); free(p); free(c); free(taken);
     return 0;
+}
+
+int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
+                 int k, int acc_double, float* logits, int32_t* idx, float* w) {
+    return oracle_route_ex(x, M, H, Wg, E, k, 0, NULL, 1.0f, acc_double, logits, idx, w);
 }
 
 /* One SwiGLU expert: g = W1 x, u = W3 x, h = silu(g) * u with

@@ -77,6 +77,18 @@ int oracle_lm_head(const uint16_t* x, int M, int H, const void* W,
 int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
                  int k, int acc_double, float* logits, int32_t* idx, float* w);
 
+/* Router with a choice of scoring, a selection bias and a scaling factor
+ * ("Chasing the Batch-1 Floor", "PDL: stacking the latency floors of small
+ * kernels": a bias read by the top-k step). scoring 0: softmax over all E;
+ * 1: the logistic function of each logit. The k experts with the largest
+ * score + bias[e] are selected (bias may be NULL; with softmax and no bias
+ * the logits themselves are ranked, the same order), ties to the lower
+ * index, in descending order; their unbiased scores are renormalised to sum
+ * to one and multiplied by routed_scale (a value <= 0 means 1). */
+int oracle_route_ex(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
+                    int k, int scoring, const float* bias, float routed_scale,
+                    int acc_double, float* logits, int32_t* idx, float* w);
+
 /* One SwiGLU expert on one token: z = W2 (silu(W1 x) * (W3 x)).
  * wfmt 0: W1/W3/W2 are bf16, s1/s3/s2 ignored. wfmt 1: MXFP4 codes + scales.
  * wfmt 2: FP8 e4m3 codes [rows, K] with fp32 scales [rows, K / 128] (the s
