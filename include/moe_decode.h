@@ -4,7 +4,8 @@
  *
  * The layer, for M = 1..16 tokens (batch-1 decode and speculative verify):
  *   logits = x Wg^T                      router gate matvec, bf16 weight
- *   p = softmax(logits); S = top-k(p); w = p_S / sum p_S
+ *   p = softmax(logits) (or sigmoid(logits)); S = top-k(p + bias);
+ *   w = routed_scale * p_S / sum p_S
  *   y_t = sum_j w_tj * E_{S_tj}(x_t) + E_shared(x_t)
  *   E(x) = W2 (silu(W1 x) * (W3 x)),   silu(g) = g / (1 + e^-g)
  * "Chasing the Batch-1 Floor: Ling-3.0-flash Speculative Decode on
@@ -116,6 +117,14 @@ typedef struct moe_shape {
     int32_t inter;        /* I: multiple of 64 (FP8: 128), at most 4096 */
     int32_t shared_inter; /* Is: 0 (no shared expert) or a multiple of 64, <= 4096 */
     int32_t wfmt;         /* routed expert weights: 0 = bf16, 1 = MXFP4, 2 = FP8 e4m3 */
+    /* router configuration ("Chasing the Batch-1 Floor", "PDL: stacking the
+     * latency floors of small kernels": the top-k step reads a selection
+     * bias). Zero-initialised fields give the plain softmax router. */
+    int32_t scoring;          /* 0: softmax over all E; 1: sigmoid of each logit */
+    float routed_scale;       /* routing weights are multiplied by this (<= 0: 1) */
+    const float* router_bias; /* NULL, or fp32 [E] (device) added to the scores
+                                 to select the top k only; the weights use
+                                 the unbiased scores, renormalised */
 } moe_shape;
 
 typedef struct moe_weights {

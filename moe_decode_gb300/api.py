@@ -27,6 +27,7 @@ F_DEBUG_FORCE_TIMEOUT = 256
 OPT_GRID_CTAS = 1
 OPT_WAIT_TIMEOUT_NS = 2
 OPT_TRACE_BUFFER = 3
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 LM_HEAD_WORKSPACE_BYTES = 1024
 STATIC_SCRATCH_BYTES = 524288
 
@@ -39,7 +40,8 @@ class MoeError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
-                ("inter", ctypes.c_int32), ("shared_inter", ctypes.c_int32), ("wfmt", ctypes.c_int32)]
+                ("inter", ctypes.c_int32), ("shared_inter", ctypes.c_int32), ("wfmt", ctypes.c_int32),
+                ("scoring", ctypes.c_int32), ("routed_scale", ctypes.c_float), ("router_bias", ctypes.c_void_p)]
 
 
 class _Weights(ctypes.Structure):
@@ -98,8 +100,12 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_shape(hidden, n_experts, top_k, inter, shared_inter, wfmt=0) -> Shape:
-    return Shape(hidden, n_experts, top_k, inter, shared_inter, wfmt)
+def make_shape(hidden, n_experts, top_k, inter, shared_inter, wfmt=0, scoring: int = 0, routed_scale: float = 0.0,
+               router_bias: Optional[torch.Tensor] = None) -> Shape:
+    """Layer shape and router configuration; router_bias (fp32 [E], device)
+    must stay alive while the shape is used."""
+    return Shape(hidden, n_experts, top_k, inter, shared_inter, wfmt, scoring, routed_scale,
+                 None if router_bias is None else router_bias.data_ptr())
 
 
 @dataclass

@@ -97,6 +97,8 @@ int check_shape(const moe_shape* s, int M) {
     if (k < 1 || k > moe::kMaxK || k > E) return MOE_ESHAPE;
     if (I <= 0 || I % (s->wfmt == 2 ? 128 : 64) != 0 || I > 4096) return MOE_ESHAPE;
     if (Is < 0 || Is % 64 != 0 || Is > 4096) return MOE_ESHAPE;
+    if (s->scoring != 0 && s->scoring != 1) return MOE_ESHAPE;
+    if (s->router_bias && (reinterpret_cast<uintptr_t>(s->router_bias) & 3u)) return MOE_EALIGN;
     return MOE_OK;
 }
 
@@ -136,6 +138,9 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.mode = mode;
     p.G = G;
     p.rpc = (p.H + G - 1) / G;
+    p.scoring = s->scoring;
+    p.routed_scale = s->routed_scale > 0.f ? s->routed_scale : 1.f;
+    p.bias = s->router_bias;
     p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
     p.trace = g_opt.trace;
     uint8_t* base = static_cast<uint8_t*>(ws);

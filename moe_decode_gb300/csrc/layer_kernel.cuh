@@ -969,38 +969,43 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Softmax, top-k (descending logit, ties to the lower expert index) and
-// renormalisation for one token, by one warp. The logits come from every CTA
-// as 64-bit words (logit, tag): the warp reads them with relaxed loads until
-// every tag is this call's (a bounded wait; no grid barrier). Lane l holds
-// the logits of experts 64j + 2l and 64j + 2l + 1 (EPL of them) and keeps its
-// own best entry; each of the k rounds takes the warp maximum with one
-// hardware reduction, the lowest expert index among the lanes holding it with
-// a second, and the winning lane rescans its entries. The code stays small on
-// purpose: it runs once per launch, so its instructions are fetched cold. The
-// full softmax denominator cancels in the renormalisation, so
-// w_j = exp(l_j - max) / sum over the selected of exp(l - max).
-// Returns false when the wait ran out (the CTA is then aborted).
-template <int EPL>
+// Scores, top-k and routing weights for one token, by one warp. The logits
+// come from every CTA as 64-bit words (logit, tag): the warp reads them with
+// relaxed loads until every tag is this call's (a bounded wait; no grid
+// barrier). Lane l holds experts 64j + 2l and 64j + 2l + 1 (EPL of them).
+//  - Plain softmax router (no bias): the logits themselves are ranked (the
+//    same order as the probabilities); w_j = exp(l_j - max) / sum over the
+//    selected of exp(l - max) (the full softmax denominator cancels).
+//  - Otherwise the scores s (softmax over all E, or the sigmoid of each
+//    logit) plus the expert's bias are ranked, and w_j = s_j / sum over the
+//    selected of s.
+// Ties go to the lower expert index; the weights are multiplied by the
+// routed scaling factor. Each of the k rounds takes the warp maximum of the
+// ranking keys with one hardware reduction and the lowest expert index
+// among the lanes holding it with a second; the winning lane drops the entry
+// and rescans. The code stays small on purpose: it runs once per launch, so
+// its instructions are fetched cold. Returns false when the wait ran out
+// (the CTA is then aborted).
+template <int EPL, bool VAR>
 __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lrow, const int E, const int k,
                                        int lane, uint32_t tag, const LayerParams& p, Plan* plan,
                                        int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
-    uint32_t key[EPL];
+    float lg[EPL];
     uint64_t t0 = 0;
     for (int spin = 0;; ++spin) {
         bool ok = true;
 #pragma unroll
         for (int j = 0; j < EPL / 2; ++j) {
             const int e = 64 * j + 2 * lane;
-            key[2 * j] = key[2 * j + 1] = 0u;
+            lg[2 * j] = lg[2 * j + 1] = -INFINITY;
             if (e < E) {
                 unsigned long long a, b;
                 ld_relaxed_v2u64(lrow + e, a, b);
                 ok = ok && (uint32_t)(a >> 32) == tag;
-                key[2 * j] = f32_key(__uint_as_float((uint32_t)a));
+                lg[2 * j] = __uint_as_float((uint32_t)a);
                 if (e + 1 < E) {
                     ok = ok && (uint32_t)(b >> 32) == tag;
-                    key[2 * j + 1] = f32_key(__uint_as_float((uint32_t)b));
+                    lg[2 * j + 1] = __uint_as_float((uint32_t)b);
                 }
             }
         }
@@ -1015,6 +1020,40 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
         __nanosleep(64);
     }
     auto idx_of = [lane](int j) { return (uint32_t)(64 * (j >> 1) + 2 * lane + (j & 1)); };
+    // VAR: unbiased scores and biased ranking keys; else the logits themselves
+    constexpr bool by_logit = !VAR;
+    float sc[EPL];
+    uint32_t key[EPL];
+    if (by_logit) {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) sc[j] = lg[j];
+    } else if (p.scoring == 0) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) mx = fmaxf(mx, lg[j]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+            sc[j] = (uint32_t)idx_of(j) < (uint32_t)E ? expf(lg[j] - mx) : 0.f;
+            den += sc[j];
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) sc[j] = sc[j] / den;
+    } else {
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) sc[j] = 1.0f / (1.0f + expf(-lg[j]));
+    }
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+        const uint32_t e = idx_of(j);
+        float kv = sc[j];
+        if (!by_logit && p.bias && e < (uint32_t)E) kv += __ldg(p.bias + e);
+        key[j] = e < (uint32_t)E ? f32_key(kv) : 0u;
+    }
     uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
@@ -1022,32 +1061,39 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
             bk = key[j];
             bi = idx_of(j);
         }
-    float mx = 0.f, mine = 0.f;
+    float mine = 0.f, first = 0.f;
     for (int jj = 0; jj < k; ++jj) {
         const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? bi : 0xffffffffu);
-        const float wv = key_f32(wk);
-        if (jj == 0) mx = wv;
-        if (lane == jj) mine = wv;
+        float ws = 0.f;
         if (lane == 0) sel_e[jj] = (int32_t)we;
-        if (we == bi) {  // this lane won: drop the entry, find the next best
+        if (we == bi) {  // this lane won: take its score, drop the entry, find the next best
             bk = 0u;
             bi = 0xffffffffu;
 #pragma unroll
             for (int j = 0; j < EPL; ++j) {
-                if (idx_of(j) == we) key[j] = 0u;
+                if (idx_of(j) == we) {
+                    ws = sc[j];
+                    key[j] = 0u;
+                }
                 if (key[j] > bk) {
                     bk = key[j];
                     bi = idx_of(j);
                 }
             }
         }
+        if (by_logit)
+            ws = key_f32(wk);  // the winning key is the logit itself
+        else
+            ws = __shfl_sync(0xffffffffu, ws, (int)((we & 63u) >> 1));  // from the winning lane
+        if (jj == 0) first = ws;
+        if (lane == jj) mine = ws;
     }
-    const float ex = lane < k ? expf(mine - mx) : 0.f;
-    float den = ex;
+    const float num = lane < k ? (by_logit ? expf(mine - first) : mine) : 0.f;
+    float den = num;
 #pragma unroll
     for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    if (lane < k) sel_w[lane] = ex / den;
+    if (lane < k) sel_w[lane] = num / den * p.routed_scale;
     return true;
 }
 
@@ -1057,10 +1103,16 @@ static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* p
     const uint32_t tag = plan->tag + (p.force_timeout ? 1u : 0u);
     for (int t = warp; t < p.M; t += nwarps) {
         const unsigned long long* lrow = p.logits + (size_t)t * p.Es;
-        const bool ok = p.E <= 512 ? topk_warp<16>(lrow, p.E, p.k, lane, tag, p, plan, plan->sel_e + t * p.k,
-                                                   plan->sel_w + t * p.k)
-                                   : topk_warp<32>(lrow, p.E, p.k, lane, tag, p, plan, plan->sel_e + t * p.k,
-                                                   plan->sel_w + t * p.k);
+        int32_t* se = plan->sel_e + t * p.k;
+        float* sw = plan->sel_w + t * p.k;
+        const bool var = p.scoring != 0 || p.bias != nullptr;
+        bool ok;
+        if (p.E <= 512)
+            ok = var ? topk_warp<16, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw)
+                     : topk_warp<16, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw);
+        else
+            ok = var ? topk_warp<32, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw)
+                     : topk_warp<32, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw);
         if (!ok) return;
     }
 }

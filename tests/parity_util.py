@@ -37,6 +37,21 @@ def near_tie(logits_row: np.ndarray, k: int) -> bool:
     return k < s.size and (s[k - 1] - s[k]) < TIE_GAP
 
 
+def ranking_keys(logits: np.ndarray, router) -> np.ndarray:
+    """What the router ranks: the logits (plain softmax router), else the
+    scores (softmax or sigmoid) plus the selection bias."""
+    if router is None or (router.get("scoring", 0) == 0 and router.get("bias") is None):
+        return logits
+    l = logits.astype(np.float64)
+    if router.get("scoring", 0) == 1:
+        s = 1.0 / (1.0 + np.exp(-l))
+    else:
+        e = np.exp(l - l.max(axis=1, keepdims=True))
+        s = e / e.sum(axis=1, keepdims=True)
+    b = router.get("bias")
+    return s + (0.0 if b is None else b.cpu().numpy().astype(np.float64))
+
+
 def check_routing(idx_gpu, w_gpu, idx_o, w_o, logits_o, k):
     """Returns the list of exempt (near-tie) tokens; asserts the rest."""
     exempt = []
@@ -56,11 +71,21 @@ def check_routing(idx_gpu, w_gpu, idx_o, w_o, logits_o, k):
     return exempt
 
 
-def oracle_layer(shape, layer: dict, x_u16: np.ndarray, wfmt: int, idx_override=None, w_override=None):
+def oracle_layer(shape, layer: dict, x_u16: np.ndarray, wfmt: int, idx_override=None, w_override=None,
+                 router=None):
     """Oracle routing + FFN on host copies of the touched experts of a device
-    layer. Returns (idx, w, logits, y)."""
+    layer. router: None (plain softmax) or a dict with scoring, bias (device
+    fp32 [E] or None) and scale. Returns (idx, w, keys, y), keys being what
+    the router ranks."""
     Wg = synth.to_u16(layer["Wg"])
-    idx, w, logits = oracle.route(x_u16, Wg, shape.top_k)
+    if router is None:
+        idx, w, logits = oracle.route(x_u16, Wg, shape.top_k)
+    else:
+        b = router.get("bias")
+        idx, w, logits = oracle.route_ex(x_u16, Wg, shape.top_k, scoring=router.get("scoring", 0),
+                                         bias=None if b is None else b.cpu().numpy(),
+                                         routed_scale=router.get("scale", 0.0))
+    logits = ranking_keys(logits, router)
     ri = idx if idx_override is None else idx_override
     rw = w if w_override is None else w_override
     experts = {int(e): synth.host_expert(shape, layer, int(e), wfmt) for e in np.unique(ri)}
@@ -76,12 +101,19 @@ def expert_weights_of(layer: dict, wfmt: int):
                              s2=layer.get("s2"))
 
 
-def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0):
+def api_shape(shape, wfmt: int, router=None):
+    from moe_decode_gb300 import api
+    r = router or {}
+    return api.make_shape(shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter, wfmt,
+                          scoring=r.get("scoring", 0), routed_scale=r.get("scale", 0.0), router_bias=r.get("bias"))
+
+
+def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0, router=None):
     """The fused layer through the C ABI. Returns (idx, w, y) on the host and
     the device status word."""
     from moe_decode_gb300 import api
     M = x.shape[0]
-    s = api.make_shape(shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter, wfmt)
+    s = api_shape(shape, wfmt, router)
     ws = api.workspace(s, M)
     idx = torch.full((M, shape.top_k), -1, dtype=torch.int32, device=x.device)
     w = torch.zeros((M, shape.top_k), dtype=torch.float32, device=x.device)
@@ -91,16 +123,16 @@ def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0):
     return idx.cpu().numpy(), w.cpu().numpy(), y, st
 
 
-def compare_layer(shape, layer, x: torch.Tensor, wfmt: int):
+def compare_layer(shape, layer, x: torch.Tensor, wfmt: int, router=None):
     """Full parity check of moe_decode_layer against the oracle."""
-    idx_g, w_g, y_g, st = run_layer(shape, layer, x, wfmt)
+    idx_g, w_g, y_g, st = run_layer(shape, layer, x, wfmt, router=router)
     assert st == 0, st
     x_u16 = synth.to_u16(x)
-    idx_o, w_o, logits_o, y_o = oracle_layer(shape, layer, x_u16, wfmt)
+    idx_o, w_o, logits_o, y_o = oracle_layer(shape, layer, x_u16, wfmt, router=router)
     exempt = check_routing(idx_g, w_g, idx_o, w_o, logits_o, shape.top_k)
     y_ref = y_o.copy()
     if exempt:
-        _, _, _, y_alt = oracle_layer(shape, layer, x_u16, wfmt, idx_override=idx_g, w_override=w_g)
+        _, _, _, y_alt = oracle_layer(shape, layer, x_u16, wfmt, idx_override=idx_g, w_override=w_g, router=router)
         y_ref[exempt] = y_alt[exempt]
     err = rel_l2(bf16_bits_to_f32(y_g), y_ref)
     assert err <= TOL_Y[wfmt], err

@@ -265,6 +265,44 @@ def test_ffn_matches_layer(api, ling):
     assert torch.equal(y, y_layer)
 
 
+# ------------------------------------------------------------------ router variants
+
+def _router(shape, kind, seed):
+    bias = synth.normal_f32(seed, 7, 0, shape.n_experts, 0.02, "cuda")
+    return {"sigmoid_bias_scale": dict(scoring=1, bias=bias, scale=2.5),
+            "sigmoid": dict(scoring=1, bias=None, scale=0.0),
+            "softmax_bias": dict(scoring=0, bias=bias * 5, scale=0.0)}[kind]
+
+
+@pytest.mark.parametrize("kind", ["sigmoid_bias_scale", "sigmoid", "softmax_bias"])
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_tiny_router_variants(tiny, kind, M):
+    x = synth.x_independent(synth.TINY, 70 + M, M, device="cuda")
+    pu.compare_layer(synth.TINY, tiny, x, 0, router=_router(synth.TINY, kind, 80 + M))
+
+
+@pytest.mark.parametrize("M", [1, 6])
+def test_ling_sigmoid_bias_router(ling, M):
+    x = synth.x_independent(synth.LING, 90 + M, M, device="cuda")
+    pu.compare_layer(synth.LING, ling, x, 0, router=_router(synth.LING, "sigmoid_bias_scale", 95 + M))
+
+
+def test_route_only_with_sigmoid_bias(api, ling):
+    M = 4
+    r = _router(synth.LING, "sigmoid_bias_scale", 99)
+    s = pu.api_shape(synth.LING, 0, r)
+    x = synth.x_independent(synth.LING, 98, M, device="cuda")
+    ws = api.workspace(s, M)
+    idx = torch.full((M, 8), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((M, 8), dtype=torch.float32, device="cuda")
+    api.route(x, ling["Wg"], s, idx, w, ws)
+    assert api.read_status(ws) == 0
+    idx_o, w_o, l_o = oracle.route_ex(synth.to_u16(x), synth.to_u16(ling["Wg"]), 8, scoring=1,
+                                      bias=r["bias"].cpu().numpy(), routed_scale=2.5)
+    pu.check_routing(idx.cpu().numpy(), w.cpu().numpy(), idx_o, w_o, pu.ranking_keys(l_o, r), 8)
+    assert np.allclose(w.cpu().numpy().sum(axis=1), 2.5, rtol=1e-5)
+
+
 # ------------------------------------------------------------------ device failure reporting
 
 def test_bounded_wait_reports_timeout_and_recovers(api, tiny):
