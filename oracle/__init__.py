@@ -53,6 +53,7 @@ def _load():
         lib.oracle_mxfp4_decode.argtypes = [P, P, i64, i32, P]
         lib.oracle_route.argtypes = [P, i32, i32, P, i32, i32, i32, P, P, P]
         lib.oracle_route_ex.argtypes = [P, i32, i32, P, i32, i32, i32, P, ctypes.c_float, i32, P, P, P]
+        lib.oracle_rmsnorm.argtypes = [P, i32, i32, P, ctypes.c_float, P]
         lib.oracle_fp8_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.oracle_fp8_e4m3_value.restype = ctypes.c_double
         lib.oracle_fp8_e4m3_encode.argtypes = [ctypes.c_float]
@@ -223,3 +224,15 @@ def lm_head(x_u16: np.ndarray, W, V: int, wfmt: int = 0, scale=None, acc_double:
     if rc:
         raise ValueError(f"oracle_lm_head: {rc}")
     return out
+
+
+def rmsnorm(h_u16: np.ndarray, gamma_u16: np.ndarray, eps: float) -> np.ndarray:
+    """x = bf16(h / sqrt(mean(h^2) + eps) * gamma) for bf16 bits h [M, H]."""
+    h = _c(h_u16, np.uint16)
+    g = _c(gamma_u16, np.uint16)
+    M, H = h.shape
+    x = np.empty((M, H), np.uint16)
+    rc = _load().oracle_rmsnorm(_ptr(h), M, H, _ptr(g), eps, _ptr(x))
+    if rc:
+        raise ValueError(f"oracle_rmsnorm rc={rc}")
+    return x

@@ -358,3 +358,40 @@ int oracle_lm_head(const uint16_t* x, int M, int H, const void* W,
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------ RMSNorm */
+/* Pre-MoE norm ("Chasing the Batch-1 Floor", "PDL: stacking the latency
+   floors of small kernels": the router chain starts with the norm):
+   x = h / sqrt(mean(h^2) + eps) * gamma, in float64, rounded once to bf16
+   (nearest, ties to even). */
+static uint16_t f64_to_bf16_rne(double v) {
+    if (isnan(v)) return 0x7fc0;
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    const double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                        /* a = m 2^e, m in [0.5, 1) */
+    const int sh = e - 1 < -126 ? 133 : 8 - e;  /* bf16 grid: 8 significant
+                                                   bits, subnormals 2^-133 */
+    const double r = ldexp(rint(ldexp(a, sh)), -sh);  /* ties to even */
+    const float f = (float)r;            /* exact (or inf beyond the range) */
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    return (uint16_t)(sign | (b >> 16));
+}
+
+int oracle_rmsnorm(const uint16_t* h, int M, int H, const uint16_t* gamma, float eps, uint16_t* x) {
+    if (!h || !gamma || !x || M < 0 || H <= 0) return -1;
+    for (int t = 0; t < M; ++t) {
+        double ss = 0.0;
+        for (int i = 0; i < H; ++i) {
+            const double v = oracle_bf16_to_f32(h[(int64_t)t * H + i]);
+            ss += v * v;
+        }
+        const double r = 1.0 / sqrt(ss / H + (double)eps);
+        for (int i = 0; i < H; ++i)
+            x[(int64_t)t * H + i] = f64_to_bf16_rne((double)oracle_bf16_to_f32(h[(int64_t)t * H + i]) * r *
+                                                    (double)oracle_bf16_to_f32(gamma[i]));
+    }
+    return 0;
+}

@@ -77,6 +77,11 @@ int oracle_lm_head(const uint16_t* x, int M, int H, const void* W,
 int oracle_route(const uint16_t* x, int M, int H, const uint16_t* Wg, int E,
                  int k, int acc_double, float* logits, int32_t* idx, float* w);
 
+/* Pre-MoE RMSNorm of M tokens of the residual stream h (bf16 [M, H]):
+ * x = h / sqrt(mean(h^2) + eps) * gamma, computed in float64 and rounded
+ * once to bf16 (nearest, ties to even). */
+int oracle_rmsnorm(const uint16_t* h, int M, int H, const uint16_t* gamma, float eps, uint16_t* x);
+
 /* Router with a choice of scoring, a selection bias and a scaling factor
  * ("Chasing the Batch-1 Floor", "PDL: stacking the latency floors of small
  * kernels": a bias read by the top-k step). scoring 0: softmax over all E;
