@@ -125,6 +125,17 @@ typedef struct moe_shape {
     const float* router_bias; /* NULL, or fp32 [E] (device) added to the scores
                                  to select the top k only; the weights use
                                  the unbiased scores, renormalised */
+    /* layer input and output ("PDL: stacking the latency floors of small
+     * kernels": the router chain starts with the norm; the residual add
+     * closes the layer). Zero-initialised fields: x is taken as given. */
+    const void* norm_weight;  /* NULL, or bf16 [H] (device, 16-byte aligned):
+                                 the input is the residual stream h and the
+                                 layer runs on x = bf16(h / sqrt(mean(h^2) +
+                                 eps) * norm_weight) */
+    float norm_eps;           /* RMSNorm epsilon (<= 0: 1e-6) */
+    int32_t residual;         /* 1: y = input + MoE(x), added in fp32 before
+                                 the single bf16 cast (moe_ffn and
+                                 moe_decode_layer) */
 } moe_shape;
 
 typedef struct moe_weights {

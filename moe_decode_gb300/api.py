@@ -41,7 +41,8 @@ class MoeError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("shared_inter", ctypes.c_int32), ("wfmt", ctypes.c_int32),
-                ("scoring", ctypes.c_int32), ("routed_scale", ctypes.c_float), ("router_bias", ctypes.c_void_p)]
+                ("scoring", ctypes.c_int32), ("routed_scale", ctypes.c_float), ("router_bias", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("residual", ctypes.c_int32)]
 
 
 class _Weights(ctypes.Structure):
@@ -101,11 +102,14 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def make_shape(hidden, n_experts, top_k, inter, shared_inter, wfmt=0, scoring: int = 0, routed_scale: float = 0.0,
-               router_bias: Optional[torch.Tensor] = None) -> Shape:
-    """Layer shape and router configuration; router_bias (fp32 [E], device)
+               router_bias: Optional[torch.Tensor] = None, norm_weight: Optional[torch.Tensor] = None,
+               norm_eps: float = 0.0, residual: bool = False) -> Shape:
+    """Layer shape, router configuration and input/output options;
+    router_bias (fp32 [E]) and norm_weight (bf16 [H]) are device tensors that
     must stay alive while the shape is used."""
     return Shape(hidden, n_experts, top_k, inter, shared_inter, wfmt, scoring, routed_scale,
-                 None if router_bias is None else router_bias.data_ptr())
+                 None if router_bias is None else router_bias.data_ptr(),
+                 None if norm_weight is None else norm_weight.data_ptr(), norm_eps, int(residual))
 
 
 @dataclass

@@ -99,6 +99,8 @@ int check_shape(const moe_shape* s, int M) {
     if (Is < 0 || Is % 64 != 0 || Is > 4096) return MOE_ESHAPE;
     if (s->scoring != 0 && s->scoring != 1) return MOE_ESHAPE;
     if (s->router_bias && (reinterpret_cast<uintptr_t>(s->router_bias) & 3u)) return MOE_EALIGN;
+    if (s->residual != 0 && s->residual != 1) return MOE_ESHAPE;
+    if (s->norm_weight && !aligned16(s->norm_weight)) return MOE_EALIGN;
     return MOE_OK;
 }
 
@@ -141,6 +143,9 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.scoring = s->scoring;
     p.routed_scale = s->routed_scale > 0.f ? s->routed_scale : 1.f;
     p.bias = s->router_bias;
+    p.gamma = static_cast<const uint16_t*>(s->norm_weight);
+    p.eps = s->norm_eps > 0.f ? s->norm_eps : 1e-6f;
+    p.residual = s->residual;
     p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
     p.trace = g_opt.trace;
     uint8_t* base = static_cast<uint8_t*>(ws);

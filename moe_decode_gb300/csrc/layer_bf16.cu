@@ -5,6 +5,8 @@
 
 namespace moe {
 cudaError_t launch_layer_bf16(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
-    return launch_persistent(moe_layer_kernel<0>, block_threads(0), p, stream, pdl, coop);
+    const bool io = p.gamma != nullptr || p.residual != 0;
+    return launch_persistent(io ? moe_layer_kernel<0, true> : moe_layer_kernel<0, false>, block_threads(0), p,
+                             stream, pdl, coop);
 }
 }  // namespace moe

@@ -6,6 +6,8 @@
 
 namespace moe {
 cudaError_t launch_layer_fp8(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
-    return launch_persistent(moe_layer_kernel<2>, block_threads(2), p, stream, pdl, coop);
+    const bool io = p.gamma != nullptr || p.residual != 0;
+    return launch_persistent(io ? moe_layer_kernel<2, true> : moe_layer_kernel<2, false>, block_threads(2), p,
+                             stream, pdl, coop);
 }
 }  // namespace moe

@@ -1171,8 +1171,83 @@ static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, int
     named_bar_sync(1, nct);
 }
 
-// ------------------------------------------------------------ the kernel
+// Tokens into shared memory, one warp per token, for the cases that need
+// arithmetic. With a norm weight g the input is the residual stream h and the
+// token is x = bf16(h / rms * g), rms = sqrt(mean(h^2) + eps). MXFP4 layers
+// hold the tokens in f16 times 2^s_t (x_inv[t] = 2^-s_t), s_t chosen from
+// the token's largest magnitude (exact for bf16 values in f16's normal
+// range). Not inlined: it runs once per launch and keeps the kernel's other
+// code compact; its arguments are plain values.
 template <int WFMT>
+__device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const uint4* __restrict__ gam, int M, int H,
+                                         float eps, uint4* __restrict__ dst, float* __restrict__ x_inv, int warp,
+                                         int lane, int nwarps) {
+    const int nvt = H / 8;
+    for (int t = warp; t < M; t += nwarps) {
+        const uint4* ht = src + (size_t)t * nvt;
+        float r = 1.f;
+        if (gam) {
+            float ss = 0.f;
+            for (int i = lane; i < nvt; i += 32) {
+                float f[8];
+                unpack8(__ldg(ht + i), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+            ss = warp_sum(ss);
+            r = 1.0f / sqrtf(ss / (float)H + eps);
+        }
+        auto token_vec = [&](int i, float (&f)[8]) {
+            unpack8(__ldg(ht + i), f);
+            if (gam) {
+                float g[8];
+                unpack8(__ldg(gam + i), g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = bf16lo(f32_to_bf16_bits(f[e] * r * g[e]));
+            }
+        };
+        if (WFMT != 1) {
+            for (int i = lane; i < nvt; i += 32) {
+                float f[8];
+                token_vec(i, f);
+                uint4 v;
+                v.x = f32_to_bf16_bits(f[0]) | ((uint32_t)f32_to_bf16_bits(f[1]) << 16);
+                v.y = f32_to_bf16_bits(f[2]) | ((uint32_t)f32_to_bf16_bits(f[3]) << 16);
+                v.z = f32_to_bf16_bits(f[4]) | ((uint32_t)f32_to_bf16_bits(f[5]) << 16);
+                v.w = f32_to_bf16_bits(f[6]) | ((uint32_t)f32_to_bf16_bits(f[7]) << 16);
+                dst[(size_t)t * nvt + i] = v;
+            }
+            continue;
+        }
+        float mx = 0.f;
+        for (int i = lane; i < nvt; i += 32) {
+            float f[8];
+            token_vec(i, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(f[e]));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int sh = f16_range_shift(mx);
+        const float sc = exp2i(sh);
+        for (int i = lane; i < nvt; i += 32) {
+            float f[8];
+            token_vec(i, f);
+            uint4 v;
+            v.x = f32x2_to_f16x2(f[0] * sc, f[1] * sc);
+            v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
+            v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
+            v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
+            dst[(size_t)t * nvt + i] = v;
+        }
+        if (lane == 0) x_inv[t] = exp2i(-sh);
+    }
+}
+
+// ------------------------------------------------------------ the kernel
+// IO: the input is normalised in the kernel and/or the residual is added
+// (compiled only into the launches that ask for it).
+template <int WFMT, bool IO>
 __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
     constexpr int NCW = consumer_warps(WFMT);
     constexpr int NCT = NCW * 32;
@@ -1246,7 +1321,10 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
-            if (WFMT != 1) {
+            if (IO) {
+                load_tokens<WFMT>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.eps, dst,
+                                  plan->x_inv, warp, lane, NCW);
+            } else if (WFMT != 1) {
                 for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
             } else {
                 // MXFP4 layers hold the tokens in f16 times 2^s_t, s_t chosen
@@ -1331,6 +1409,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                     float v = p.Is > 0 ? ypair[(size_t)t * p.rpc + r] : 0.f;
                     for (int q = 0; q < npr; ++q)
                         if (plan->pair_tok[q] == t) v = fmaf(plan->pair_w[q], ypair[(size_t)(p.M + q) * p.rpc + r], v);
+                    if (IO && p.residual) v += bf16lo(p.x[(size_t)t * p.H + h0 + r]);  // the layer's input
                     p.y[(size_t)t * p.H + h0 + r] = f32_to_bf16_bits(v);
                 }
             }

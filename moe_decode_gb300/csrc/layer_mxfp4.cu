@@ -7,7 +7,9 @@
 
 namespace moe {
 cudaError_t launch_layer_mxfp4(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
-    return launch_persistent(moe_layer_kernel<1>, block_threads(1), p, stream, pdl, coop);
+    const bool io = p.gamma != nullptr || p.residual != 0;
+    return launch_persistent(io ? moe_layer_kernel<1, true> : moe_layer_kernel<1, false>, block_threads(1), p,
+                             stream, pdl, coop);
 }
 
 __global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,

@@ -51,6 +51,9 @@ struct LayerParams {
     int Es;
     uint16_t* hs;          // shared-expert activations [M, Is] bf16
     uint16_t* hr;          // routed activations [M*k, I] bf16, grouped by expert
+    const uint16_t* gamma; // RMSNorm weight [H] bf16, or null (x taken as given)
+    float eps;             // RMSNorm epsilon
+    int residual;          // 1: y += input
     const float* bias;     // router selection bias [E], may be null
     float routed_scale;    // routing-weight factor (1 for none)
     int scoring;           // 0 softmax, 1 sigmoid

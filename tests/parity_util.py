@@ -101,19 +101,21 @@ def expert_weights_of(layer: dict, wfmt: int):
                              s2=layer.get("s2"))
 
 
-def api_shape(shape, wfmt: int, router=None):
+def api_shape(shape, wfmt: int, router=None, io=None):
     from moe_decode_gb300 import api
     r = router or {}
+    o = io or {}
     return api.make_shape(shape.hidden, shape.n_experts, shape.top_k, shape.inter, shape.shared_inter, wfmt,
-                          scoring=r.get("scoring", 0), routed_scale=r.get("scale", 0.0), router_bias=r.get("bias"))
+                          scoring=r.get("scoring", 0), routed_scale=r.get("scale", 0.0), router_bias=r.get("bias"),
+                          norm_weight=o.get("gamma"), norm_eps=o.get("eps", 0.0), residual=o.get("residual", False))
 
 
-def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0, router=None):
+def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0, router=None, io=None):
     """The fused layer through the C ABI. Returns (idx, w, y) on the host and
     the device status word."""
     from moe_decode_gb300 import api
     M = x.shape[0]
-    s = api_shape(shape, wfmt, router)
+    s = api_shape(shape, wfmt, router, io)
     ws = api.workspace(s, M)
     idx = torch.full((M, shape.top_k), -1, dtype=torch.int32, device=x.device)
     w = torch.zeros((M, shape.top_k), dtype=torch.float32, device=x.device)
@@ -123,17 +125,26 @@ def run_layer(shape, layer: dict, x: torch.Tensor, wfmt: int, flags: int = 0, ro
     return idx.cpu().numpy(), w.cpu().numpy(), y, st
 
 
-def compare_layer(shape, layer, x: torch.Tensor, wfmt: int, router=None):
-    """Full parity check of moe_decode_layer against the oracle."""
-    idx_g, w_g, y_g, st = run_layer(shape, layer, x, wfmt, router=router)
+def compare_layer(shape, layer, x: torch.Tensor, wfmt: int, router=None, io=None):
+    """Full parity check of moe_decode_layer against the oracle. io: None or
+    a dict with gamma (device bf16 [H]), eps and residual: the input x is
+    then the residual stream, normalised by the oracle's RMSNorm, and the
+    expected output includes the residual."""
+    idx_g, w_g, y_g, st = run_layer(shape, layer, x, wfmt, router=router, io=io)
     assert st == 0, st
-    x_u16 = synth.to_u16(x)
+    h_u16 = synth.to_u16(x)
+    x_u16 = h_u16
+    if io and io.get("gamma") is not None:
+        eps = io.get("eps", 0.0)
+        x_u16 = oracle.rmsnorm(h_u16, synth.to_u16(io["gamma"]), eps if eps > 0 else 1e-6)
     idx_o, w_o, logits_o, y_o = oracle_layer(shape, layer, x_u16, wfmt, router=router)
     exempt = check_routing(idx_g, w_g, idx_o, w_o, logits_o, shape.top_k)
     y_ref = y_o.copy()
     if exempt:
         _, _, _, y_alt = oracle_layer(shape, layer, x_u16, wfmt, idx_override=idx_g, w_override=w_g, router=router)
         y_ref[exempt] = y_alt[exempt]
+    if io and io.get("residual"):
+        y_ref = y_ref + oracle.bf16_to_f32(h_u16)
     err = rel_l2(bf16_bits_to_f32(y_g), y_ref)
     assert err <= TOL_Y[wfmt], err
     return err, idx_g, exempt

@@ -303,6 +303,44 @@ def test_route_only_with_sigmoid_bias(api, ling):
     assert np.allclose(w.cpu().numpy().sum(axis=1), 2.5, rtol=1e-5)
 
 
+# ------------------------------------------------------------------ fused norm and residual
+
+def _io(shape, seed, norm=True, residual=True, eps=1e-6):
+    g = synth.normal_bf16(seed, 8, 0, shape.hidden, 1.0, "cuda") if norm else None
+    return dict(gamma=g, eps=eps, residual=residual)
+
+
+@pytest.mark.parametrize("norm,residual", [(True, True), (True, False), (False, True)])
+@pytest.mark.parametrize("M", [1, 7])
+def test_tiny_norm_and_residual(tiny, norm, residual, M):
+    h = synth.normal_bf16(110 + M, 9, 0, M * synth.TINY.hidden, 3.0, "cuda").view(M, synth.TINY.hidden)
+    pu.compare_layer(synth.TINY, tiny, h, 0, io=_io(synth.TINY, 120 + M, norm, residual))
+
+
+@pytest.mark.parametrize("M", [1, 6])
+def test_ling_norm_residual(ling, M):
+    h = synth.normal_bf16(130 + M, 9, 0, M * 2560, 3.0, "cuda").view(M, 2560)
+    pu.compare_layer(synth.LING, ling, h, 0, io=_io(synth.LING, 140 + M))
+
+
+def test_mxfp4_norm_residual(ling_mxfp4):
+    h = synth.normal_bf16(150, 9, 0, 3 * 2560, 3.0, "cuda").view(3, 2560)
+    pu.compare_layer(synth.LING, ling_mxfp4, h, 1, io=_io(synth.LING, 151))
+
+
+def test_residual_with_zero_experts_returns_the_input(api):
+    """All expert weights zero: y = h exactly (the residual passes through
+    one fp32 add of zero and one bf16 rounding)."""
+    sh = synth.TINY
+    layer = synth.device_layer(sh, 5)
+    for n in ("w1", "w3", "w2", "ws1", "ws3", "ws2"):
+        layer[n].zero_()
+    h = synth.normal_bf16(160, 9, 0, 4 * sh.hidden, 3.0, "cuda").view(4, sh.hidden)
+    _, _, y, st = pu.run_layer(sh, layer, h, 0, io=_io(sh, 161, norm=True, residual=True))
+    assert st == 0
+    assert torch.equal(y, h)
+
+
 # ------------------------------------------------------------------ device failure reporting
 
 def test_bounded_wait_reports_timeout_and_recovers(api, tiny):
