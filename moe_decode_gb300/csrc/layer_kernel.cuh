@@ -44,17 +44,9 @@ namespace moe {
 
 constexpr uint32_t SB = kStageBytes;
 
-// A unit of the ring: the tiles one stage holds.
-struct Chunk {
-    int kind;   // 0 router rows, 1 gate/up rows, 2 down rows
-    int slot;   // -1 shared expert, else routed slot
-    int r0, n;  // first row and row count
-    int p0, np; // down: pair range within the slot
-};
-
 // ------------------------------------------------------------ chunk lists
-// The producer and the consumers step identical ChunkGen instances, so both
-// sides agree on every chunk. Phases: 0 router rows, 1 shared-expert gate/up
+// The producer steps ChunkGen and writes each chunk's descriptor next to its
+// stage; the consumers read the descriptors and run no generator. Phases: 0 router rows, 1 shared-expert gate/up
 // rows, 2 routed gate/up rows (needs the plan), 3 down rows (needs the plan).
 // next() returns false at the end of each phase; begin(ph) starts a phase.
 template <int WFMT>
@@ -289,9 +281,23 @@ struct Producer {
         }
     }
 
+    // Ends a phase: a stage with a descriptor and no data. While activation
+    // copies wait for barrier 2 (after the down chunks), the stage wait polls
+    // the barrier: those stages are freed only once their copies are issued.
+    __device__ __forceinline__ bool issue_end() {
+        if (aborted(plan)) return false;
+        if (!acquire(plan->npend > 0)) return false;
+        plan->desc[ring.s] = Chunk{3, 0, 0, 0, 0, 0};
+        mbar_arrive(ring.full());
+        ring.advance();
+        if (plan->npend == 0) complete_upto = ring.n;
+        return true;
+    }
+
     __device__ __forceinline__ bool issue(const Chunk& ch) {
         if (aborted(plan)) return false;
         if (!acquire(ch.kind == 2)) return false;
+        plan->desc[ring.s] = ch;
         const uint32_t dst = ring.stage(), bar = ring.full();
         bool deferred = false;
         if (ch.kind == 0) {
@@ -709,6 +715,7 @@ struct Consumer {
     int q;               // running row counter (row ownership)
     int h0;              // first output row of this CTA
     int c3;              // down chunks seen so far
+    int dg;              // parts a down chunk is split into
 
     __device__ __forceinline__ bool wait_full() { return mbar_wait(ring.full(), ring.ph, p, plan); }
     __device__ __forceinline__ void release() {
@@ -812,8 +819,10 @@ struct Consumer {
     // time. Each (pair, row) result is written exactly once, unweighted, into
     // ypair; the weighted combine runs after the last chunk, in pair order.
     __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
-        const int DG = (NCW + p.ns - 1) / p.ns;
+        const int DG = dg;
         const int c = c3++;
+        // this warp's parts are j with (c * DG + j) % NCW == warp
+        if ((uint32_t)((warp - (c * DG) % NCW + NCW) % NCW) >= (uint32_t)DG) return;
         const bool shared = ch.slot < 0;
         const int gbase = (shared ? 0 : p.M + plan->slot_p0[ch.slot]) + ch.p0;  // pair index of q0 = 0
         size_t sofs = 0;
@@ -942,18 +951,25 @@ struct Consumer {
         }
     }
 
-    // Waits for the next chunk, computes this warp's share, frees the stage.
-    __device__ __forceinline__ bool consume(const Chunk& ch) {
-        if (!wait_full()) return false;
-        const uint8_t* st = stage_ptr();
-        if (ch.kind == 0)
-            router(ch, st);
-        else if (ch.kind == 1)
-            gateup(ch, st);
-        else
-            down(ch, st);
-        release();
-        return true;
+    // Consumes the chunks of one phase, up to its end marker: waits for each
+    // stage, reads its descriptor, computes this warp's share, frees it.
+    __device__ __forceinline__ bool consume_phase() {
+        while (true) {
+            if (!wait_full()) return false;
+            const Chunk ch = plan->desc[ring.s];
+            if (ch.kind == 3) {
+                release();
+                return true;
+            }
+            const uint8_t* st = stage_ptr();
+            if (ch.kind == 0)
+                router(ch, st);
+            else if (ch.kind == 1)
+                gateup(ch, st);
+            else
+                down(ch, st);
+            release();
+        }
     }
 };
 
@@ -1288,9 +1304,12 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             trace_mark(p, 8);
             Producer<WFMT> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u};
             bool ok = true;
-            // producer-independent tiles: router rows, shared-expert gate/up rows
-            if (has_route)
+            // producer-independent tiles: router rows, shared-expert gate/up
+            // rows; an end marker closes each phase of the consumers
+            if (has_route) {
                 for (gen.begin(0, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
+                if (ok) ok = pr.issue_end();
+            }
             if (has_ffn)
                 for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
             trace_mark(p, 9);
@@ -1300,9 +1319,11 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                 trace_mark(p, 10);
                 if (ok)
                     for (gen.begin(2, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
+                if (ok) ok = pr.issue_end();
                 trace_mark(p, 11);
                 if (ok)
                     for (gen.begin(3, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
+                if (ok) ok = pr.issue_end();
                 trace_mark(p, 12);
                 if (ok) ok = pr.poll_b2(true);
                 trace_mark(p, 13);
@@ -1314,7 +1335,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         // ---------------- consumers
         const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
-        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0, 0};
+        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0, 0, (NCW + p.ns - 1) / p.ns};
         pdl_wait();
         if (tid == 0) plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
         {
@@ -1366,7 +1387,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         if (tid == 0) trace_mark(p, 1);
         bool ok = true;
         if (has_route) {
-            for (gen.begin(0, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            ok = cs.consume_phase();
             if (tid == 0) trace_mark(p, 2);
             // no grid barrier: each token's warp waits for the tagged logits
             if (!aborted(plan)) topk_tokens(p, plan, warp, lane, NCW);
@@ -1388,15 +1409,14 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
             cs.q = 0;
-            for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
-            for (gen.begin(2, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            if (ok) ok = cs.consume_phase();  // shared, then routed gate/up
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
                 atomicAdd(p.ctrl + kCtlBar2, 1u);
             }
-            for (gen.begin(3, p, plan, cta); ok && gen.next(p, plan, ch);) ok = cs.consume(ch);
+            if (ok) ok = cs.consume_phase();  // down
             named_bar_sync(1, NCT);
             if (tid == 0) trace_mark(p, 7);
             if (!aborted(plan)) {

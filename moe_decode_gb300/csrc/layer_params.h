@@ -68,8 +68,21 @@ struct LayerParams {
     uint32_t off_bar, off_plan, off_x, off_yacc, smem_bytes;
 };
 
+// A unit of the ring: the tiles one stage holds. kind 0 router rows, 1
+// gate/up rows, 2 down rows, 3 end of a phase (no data).
+struct Chunk {
+    int32_t kind;
+    int32_t slot;    // -1 shared expert, else routed slot
+    int32_t r0, n;   // first row and row count
+    int32_t p0, np;  // down: pair range within the slot
+};
+
 // Expert plan, rebuilt by every CTA after routing.
 struct Plan {
+    // the chunk each ring stage holds, written by the producer before it
+    // issues the stage's copies and read by the consumers after the stage's
+    // full barrier
+    Chunk desc[kMaxStages];
     int32_t sel_e[kMaxEntries];   // routing, token-major [M][k]
     float sel_w[kMaxEntries];
     int32_t rank[kMaxEntries];
