@@ -11,8 +11,9 @@
 //            Every CTA then waits for all tagged logits, computes softmax /
 //            top-k / renormalisation for all M tokens and builds the expert
 //            plan (distinct experts and their token lists) in shared memory.
-//   phase 1  gate/up + SwiGLU: the intermediate rows of the shared expert and
-//            of every touched routed expert are split evenly over the CTAs;
+//   phase 1  gate/up + SwiGLU: the intermediate rows of the shared expert are
+//            split evenly over the CTAs, those of the touched routed experts
+//            are claimed chunk by chunk from a global counter;
 //            h = silu(W1 x) * (W3 x) goes to the workspace in bf16.
 //                                                       -> grid barrier 2
 //   phase 2  down projection + weighted combine: CTA c owns output rows
@@ -1260,6 +1261,30 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
     }
 }
 
+// Routed gate/up rows, scheduled dynamically: the rows of all slots form one
+// list of chunks (slot by slot, cap row pairs each), and every CTA's
+// producer claims the next chunk from a global counter, so that CTAs that
+// run ahead take more. Two claims are kept in flight to hide the atomic's
+// latency. Which CTA computes a row does not change its result.
+template <int WFMT>
+__device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT>& pr, const LayerParams& p, Plan* plan) {
+    const uint32_t cap = (uint32_t)gateup_cap<WFMT>(p, true), I = (uint32_t)p.I;
+    const uint32_t cps = (I + cap - 1) / cap;  // chunks per slot
+    const uint32_t U = (uint32_t)plan->nslot * cps;
+    unsigned* wc = p.ctrl + kCtlWork;
+    uint32_t a = atomicAdd(wc, 1u), b = atomicAdd(wc, 1u);
+    bool ok = true;
+    while (ok && a < U) {
+        const uint32_t slot = a / cps, r0 = (a - slot * cps) * cap;
+        const Chunk c{1, (int)slot, (int)r0, (int)min(cap, I - r0), 0, 0};
+        const uint32_t nxt = atomicAdd(wc, 1u);
+        ok = pr.issue(c);
+        a = b;
+        b = nxt;
+    }
+    return ok;
+}
+
 // ------------------------------------------------------------ the kernel
 // IO: the input is normalised in the kernel and/or the residual is added
 // (compiled only into the launches that ask for it).
@@ -1317,8 +1342,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             if (ok && has_ffn) {
                 ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
-                if (ok)
-                    for (gen.begin(2, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
+                if (ok) ok = issue_routed_gateup(pr, p, plan);
                 if (ok) ok = pr.issue_end();
                 trace_mark(p, 11);
                 if (ok)
@@ -1442,6 +1466,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
         if (old == (unsigned)p.G - 1u) {
             atomicExch(p.ctrl + kCtlBar2, 0u);
+            atomicExch(p.ctrl + kCtlWork, 0u);
             atomicAdd(p.ctrl + kCtlEpoch, 1u);  // the next call's tag
             atomicExch(p.ctrl + kCtlExit, 0u);
         }

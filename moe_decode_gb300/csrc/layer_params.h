@@ -18,11 +18,13 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
 
 // workspace control block (uint32 words, 128 bytes apart): status, launch
-// epoch (advanced by the last CTA of every call), grid barrier, exit counter
+// epoch (advanced by the last CTA of every call), grid barrier, exit counter,
+// work counter
 constexpr int kCtlStatus = 0;
 constexpr int kCtlEpoch = 32;
 constexpr int kCtlBar2 = 64;
 constexpr int kCtlExit = 96;
+constexpr int kCtlWork = 128;  // next routed gate/up chunk to claim
 constexpr uint32_t kCtlBytes = 1024;
 
 enum : int { kModeRoute = 1, kModeFfn = 2, kModeLayer = 3 };
