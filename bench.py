@@ -350,27 +350,77 @@ class _Null:
         pass
 
 
-def time_e2e(wl: Workload, K: int, stream):
-    """Same metric through the public API with host buffers: each step copies
-    its tokens host->device (pinned) and reads y back device->host."""
+def time_e2e(wl: Workload, K: int, stream, zero_copy: bool):
+    """Same metric through the public API with host buffers, the tokens of
+    each step in pinned host memory and y read back to pinned host memory.
+    zero_copy: the host buffers are handed to the call itself, and the
+    kernel reads the tokens from, and writes y to, host memory over the
+    coherent CPU-GPU link (no copy launches); otherwise each step issues a
+    host->device copy of its tokens and a device->host copy of y around the
+    call."""
     xh = wl.xs.cpu().pin_memory()
     yh = torch.empty_like(wl.y, device="cpu").pin_memory()
     xd = torch.empty_like(wl.xs[0])
-    for s in range(8):
-        xd.copy_(xh[s % PERIOD], non_blocking=True)
-        wl.step(s, stream, x=xd)
-        yh.copy_(wl.y, non_blocking=True)
+
+    def one(s):
+        if zero_copy:
+            wl.step(s, stream, x=xh[s % PERIOD], y=yh)
+        else:
+            xd.copy_(xh[s % PERIOD], non_blocking=True)
+            wl.step(s, stream, x=xd)
+            yh.copy_(wl.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(8):
+            one(s)
     torch.cuda.synchronize()
+    graphs = None
+    if zero_copy:
+        # the steps replayed as CUDA graphs, as in the device timing: each
+        # replay's kernels still read and write the host buffers
+        try:
+            n = min(PERIOD, K)
+            gs = []
+            for cnt in (n, K % n):
+                if cnt == 0:
+                    gs.append(None)
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    g.capture_begin()
+                    try:
+                        for s in range(cnt):
+                            one(s)
+                    finally:
+                        g.capture_end()
+                gs.append(g)
+            graphs = (gs[0], K // n, gs[1])
+            graphs[0].replay()
+            torch.cuda.synchronize()
+        except Exception as e:
+            torch.cuda.synchronize()
+            print(f"# e2e graph capture failed ({e}); timing stream launches", file=sys.stderr)
+            graphs = None
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for s in range(K):
-            xd.copy_(xh[s % PERIOD], non_blocking=True)
-            wl.step(s, stream, x=xd)
-            yh.copy_(wl.y, non_blocking=True)
+        if graphs:
+            full, reps, tail = graphs
+            for _ in range(reps):
+                full.replay()
+            if tail is not None:
+                tail.replay()
+        else:
+            for s in range(K):
+                one(s)
         e1.record(stream)
     torch.cuda.synchronize()
+    if zero_copy:  # the host copy of y is the device result of the last step
+        wl.step((K - 1) % PERIOD, stream, x=xh[(K - 1) % PERIOD])
+        stream.synchronize()
+        if not torch.equal(yh, wl.y.cpu()):
+            raise RuntimeError("zero-copy result differs from the device-buffer result")
     ms = e0.elapsed_time(e1)
     return ms, xh[0].numel() * xh.element_size(), yh.numel() * yh.element_size()
 
@@ -478,9 +528,13 @@ def main():
                "weights_gb": wl.weight_bytes / 1e9}
         if main_run:
             res["clocks"] = sampler.summary()
-            e2e_ms, h2d, d2h = time_e2e(wl, K, stream)
+            e2e_ms, h2d, d2h = time_e2e(wl, K, stream, zero_copy=True)
+            e2c_ms, _, _ = time_e2e(wl, K, stream, zero_copy=False)
             res["e2e"] = {"value": e2e_ms * 1e3 / K, "unit": "us/step", "h2d_bytes_per_step": h2d,
-                          "d2h_bytes_per_step": d2h}
+                          "d2h_bytes_per_step": d2h,
+                          "mode": "zero-copy: the call gets the pinned host buffers; the kernel reads the tokens "
+                                  "and writes y over the coherent CPU-GPU link (steps replayed as CUDA graphs)",
+                          "explicit_copies_us_per_step": e2c_ms * 1e3 / K}
             if rank == 0:
                 res["cpu_steps"] = args.cpu_steps or cpu_steps_for(name)
                 res["cpu_us"] = oracle_sample(wl, res["cpu_steps"])

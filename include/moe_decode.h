@@ -19,8 +19,11 @@
  * (MXFP4 expert weights).
  *
  * Conventions for every entry point:
- *  - Pointers named as device pointers must be device (HBM) memory owned by
- *    the caller, 16-byte aligned. The library allocates and frees nothing.
+ *  - Pointers named as device pointers must be memory the GPU can address,
+ *    owned by the caller, 16-byte aligned: normally HBM. The tokens x and
+ *    the outputs y, idx_out, w_out may also be pinned host memory (on a
+ *    coherent CPU-GPU link the kernel then reads and writes it directly,
+ *    with no separate copy). The library allocates and frees nothing.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream) and never synchronise, except moe_read_status.
  *  - Return value: MOE_OK (0), or a negative MOE_E* code. A negative code
