@@ -360,3 +360,22 @@ def test_bounded_wait_reports_timeout_and_recovers(api, tiny):
     assert api.read_status(ws) == 0
     _, _, _, y_o = pu.oracle_layer(synth.TINY, tiny, synth.to_u16(x), 0)
     assert pu.rel_l2(pu.bf16_bits_to_f32(y), y_o) <= 1e-2
+
+
+# ------------------------------------------------------------------ host buffers
+
+def test_tokens_and_output_in_pinned_host_memory(api, ling):
+    """x read from and y written to pinned host memory by the kernel itself
+    (coherent CPU-GPU link): bit-equal to the device-buffer call."""
+    M = 3
+    x = synth.x_independent(synth.LING, 170, M, device="cuda")
+    _, _, y_dev, st = pu.run_layer(synth.LING, ling, x, 0)
+    assert st == 0
+    s = pu.api_shape(synth.LING, 0)
+    ws = api.workspace(s, M)
+    xh = x.cpu().pin_memory()
+    yh = torch.zeros((M, 2560), dtype=torch.bfloat16).pin_memory()
+    api.decode_layer(xh, ling["Wg"], pu.expert_weights_of(ling, 0), s, yh, ws)
+    assert api.read_status(ws) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(yh, y_dev.cpu())
