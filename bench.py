@@ -460,6 +460,20 @@ def oracle_sample(wl: Workload, nsteps: int):
     return dt / nsteps * 1e6
 
 
+def replica_timing(ms_local: float, K: int, world: int, device=None):
+    """(job us per step, replica us per step). Every rank runs its own replica
+    of the layer (the path has no exchange step), so the job's timed region is
+    the slowest rank's (max over ranks) and N replicas complete N steps in it."""
+    ms = ms_local
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us_rep = ms * 1e3 / K
+    return us_rep / world, us_rep
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -515,14 +529,9 @@ def main():
         st = wl.api.read_status(wl.ws, stream)
         if st != 0:
             raise RuntimeError(f"{name}: device status {st}")
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms], device=device, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        us_step = ms * 1e3 / K
+        us_job, us_step = replica_timing(ms, K, world, device)
         nbytes = wl.mean_bytes(K)
-        res = {"us_per_step": us_step / world, "us_per_step_per_replica": us_step,
+        res = {"us_per_step": us_job, "us_per_step_per_replica": us_step,
                "hbm_gbs": nbytes / (us_step * 1e-6) / 1e9, "bytes_per_step": nbytes,
                "distinct_experts_mean": float(np.mean(wl.distinct)), "steps": K, "launch": mode,
                "weights_gb": wl.weight_bytes / 1e9}
