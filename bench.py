@@ -45,6 +45,7 @@ WORKLOADS = {
     # small case for detailed profiler captures: the Ling layer cut to 128
     # experts (1.5 GB per copy), still far above L2
     "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128),
+    "mxfp4_e128_m6": dict(M=6, wfmt=1, copies=2, gen="independent", E=128),
 }
 
 

@@ -45,6 +45,20 @@ namespace moe {
 
 constexpr uint32_t SB = kStageBytes;
 
+// Bank-conflict-free layout of the token rows (shared memory) and of the
+// routed activation rows (workspace, copied row by row into the ring) for
+// the MXFP4 and FP8 layers, whose dot products give each lane a whole
+// block of consecutive 16-byte vectors (four for MXFP4, two for FP8), so
+// that lanes are 64 or 32 bytes apart: vector v of a row is stored at
+// v ^ ((v >> 3) & XM). The eight lanes of a quarter warp then hit eight
+// different 16-byte bank groups both for block-wise reads and for plain
+// one-vector-per-lane reads (router, shared expert). XM only flips bits of
+// v inside an aligned group of four vectors, so a row of a multiple of four
+// vectors maps onto itself. bf16 layers (XM = 0) keep the plain layout.
+template <int WFMT>
+constexpr int kXM = WFMT == 1 ? 3 : WFMT == 2 ? 1 : 0;
+__device__ __forceinline__ int swz_vec(int v, int xm) { return v ^ ((v >> 3) & xm); }
+
 // ------------------------------------------------------------ chunk lists
 // The producer steps ChunkGen and writes each chunk's descriptor next to its
 // stage; the consumers read the descriptors and run no generator. Phases: 0 router rows, 1 shared-expert gate/up
@@ -429,7 +443,7 @@ __device__ __forceinline__ void unpack8x(const uint4 v, float (&f)[8]) {
 // acc[t] = row . x_t (bf16 weights, bf16 or (XH) f16 activations, fp32
 // accumulate) over nvec 16-byte vectors; this lane takes vectors lane,
 // lane + STRIDE, ...
-template <int NT, int STRIDE = 32, bool XH = false>
+template <int NT, int STRIDE = 32, bool XH = false, int XM = 0>
 __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                          const uint4* __restrict__ x1, int nvec, int lane, float (&acc)[NT]) {
     float pa[NT][4];
@@ -442,7 +456,7 @@ __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const ui
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             float fx[8];
-            unpack8x<XH>((t == 0 ? x0 : x1)[v], fx);
+            unpack8x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
 #pragma unroll
             for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
         }
@@ -451,7 +465,7 @@ __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const ui
 }
 
 // Gate and up rows against the same tokens.
-template <int NT, bool XH = false>
+template <int NT, bool XH = false, int XM = 0>
 __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const uint4* __restrict__ r3,
                                           const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nvec,
                                           int lane, float (&g)[NT], float (&u)[NT]) {
@@ -466,7 +480,7 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             float fx[8];
-            unpack8x<XH>((t == 0 ? x0 : x1)[v], fx);
+            unpack8x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 pg[t][e & 3] = fmaf(f1[e], fx[e], pg[t][e & 3]);
@@ -560,24 +574,26 @@ __device__ __forceinline__ void dot2_mxh(const uint4* __restrict__ c1, const uin
         decode_block(c1[b], w1);
         decode_block(c3[b], w3);
         const float sc1 = e8m0_to_f32(s1[b]), sc3 = e8m0_to_f32(s3[b]);
+        const int r = (b >> 1) & 3;  // the block's swizzle (kXM<1>)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const uint4* xb = (t == 0 ? x0 : x1) + 4 * b;
-            const uint4 a[4] = {xb[0], xb[1], xb[2], xb[3]};
+            const uint4 a[4] = {xb[r], xb[1 ^ r], xb[2 ^ r], xb[3 ^ r]};
             g[t] = fmaf(block_h(w1, a), sc1, g[t]);
             u[t] = fmaf(block_h(w3, a), sc3, u[t]);
         }
     }
 }
 
-// One bf16 activation block (32 values, four uint4) as f16 times 2^s, s
-// chosen from the block's own largest magnitude; returns 2^-s.
-__device__ __forceinline__ float block_to_f16(const uint4* __restrict__ src, uint4 (&a)[4]) {
+// One bf16 activation block (32 values, four uint4 stored in the order
+// k ^ r) as f16 times 2^s, s chosen from the block's own largest magnitude;
+// returns 2^-s.
+__device__ __forceinline__ float block_to_f16(const uint4* __restrict__ src, int r, uint4 (&a)[4]) {
     float f[32];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         float t8[8];
-        unpack8(src[k], t8);
+        unpack8(src[k ^ r], t8);
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[8 * k + e] = t8[e];
     }
@@ -610,7 +626,7 @@ __device__ __forceinline__ void dot4_mxh(const uint8_t* const (&crow)[4], const 
         uint4 a[NT][4];
         float inv[NT];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) inv[t] = block_to_f16((t == 0 ? h0 : h1) + 4 * b, a[t]);
+        for (int t = 0; t < NT; ++t) inv[t] = block_to_f16((t == 0 ? h0 : h1) + 4 * b, (b >> 1) & 3, a[t]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t w[16];
@@ -644,9 +660,10 @@ __device__ __forceinline__ void dot2_fp8(const uint4* __restrict__ c1, const flo
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const uint4* xt = t == 0 ? x0 : x1;
+            const int r = (v >> 2) & 1;  // the vector pair's swizzle (kXM<2>)
             float fa[8], fb[8];
-            unpack8(xt[2 * v], fa);
-            unpack8(xt[2 * v + 1], fb);
+            unpack8(xt[2 * v + r], fa);
+            unpack8(xt[2 * v + (1 ^ r)], fb);
             float pg0 = 0.f, pg1 = 0.f, pu0 = 0.f, pu1 = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -676,9 +693,10 @@ __device__ __forceinline__ void dot4_fp8(const uint8_t* const (&crow)[4], const 
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const uint4* ht = t == 0 ? h0 : h1;
+            const int r = (v >> 2) & 1;  // the vector pair's swizzle (kXM<2>)
             float a8[8], b8[8];
-            unpack8(ht[2 * v], a8);
-            unpack8(ht[2 * v + 1], b8);
+            unpack8(ht[2 * v + r], a8);
+            unpack8(ht[2 * v + (1 ^ r)], b8);
 #pragma unroll
             for (int e = 0; e < 8; ++e) fh[t][e] = a8[e], fh[t][8 + e] = b8[e];
         }
@@ -713,7 +731,8 @@ struct Consumer {
     const uint16_t* xs;  // tokens in shared memory [M][H]
     float* ypair;        // down results per (pair, output row) [M + M*k][rpc]
     int warp, lane;
-    int q;               // running row counter (row ownership)
+    int qm;              // rows go round-robin over the warps, continuing
+                         // across chunks: the running row count mod NCW
     int h0;              // first output row of this CTA
     int c3;              // down chunks seen so far
     int dg;              // parts a down chunk is split into
@@ -723,6 +742,13 @@ struct Consumer {
         __syncwarp();
         if (lane == 0) mbar_arrive(ring.empty());
         ring.advance();
+    }
+    // First row of a chunk of n rows that this warp owns (then every NCW-th
+    // row); advances the running count past the chunk.
+    __device__ __forceinline__ int claim_rows(int n) {
+        const int j0 = warp >= qm ? warp - qm : warp - qm + NCW;
+        qm = (qm + n) % NCW;
+        return j0;
     }
     __device__ __forceinline__ const uint8_t* stage_ptr() const {
         return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(ring.stage()));
@@ -734,13 +760,12 @@ struct Consumer {
     // Router rows: logits[t][e] = Wg[e] . x_t, one warp per row.
     __device__ __forceinline__ void router(const Chunk& ch, const uint8_t* st) {
         const int nvec = p.H / 8;
-        for (int j = 0; j < ch.n; ++j, ++q) {
-            if (q % NCW != warp) continue;
+        for (int j = claim_rows(ch.n); j < ch.n; j += NCW) {
             const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             for (int t = 0; t < p.M; ++t) {
                 float acc[1];
                 const uint4* xt = xrow(t);
-                dot_bf16<1, 32, WFMT == 1>(row, xt, xt, nvec, lane, acc);
+                dot_bf16<1, 32, WFMT == 1, kXM<WFMT>>(row, xt, xt, nvec, lane, acc);
                 acc[0] = warp_sum(acc[0]);
                 if (WFMT == 1) acc[0] *= plan->x_inv[t];
                 // the logit and this call's tag in one 64-bit word: readers
@@ -758,7 +783,7 @@ struct Consumer {
         if (WFMT == 0 || shared) {
             const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
-            dot2_bf16<NT, WFMT == 1>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
+            dot2_bf16<NT, WFMT == 1, kXM<WFMT>>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
         } else {
             const size_t cb = (size_t)p.H / (WFMT == 1 ? 2 : 1), sbytes = (size_t)p.H / 32;
             const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
@@ -776,13 +801,18 @@ struct Consumer {
     // Gate/up rows: one warp per row pair, all tokens of the slot; stores
     // h = silu(g) * u in bf16.
     __device__ __forceinline__ void gateup(const Chunk& ch, const uint8_t* st) {
+        const int j0 = claim_rows(ch.n);
+        if (j0 >= ch.n) return;
         const bool shared = ch.slot < 0;
         const int inter = shared ? p.Is : p.I;
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
         const int npairs = shared ? p.M : plan->slot_p0[ch.slot + 1] - pbase;
-        uint16_t* hdst = (shared ? p.hs : p.hr) + (size_t)pbase * inter + ch.r0;
-        for (int j = 0; j < ch.n; ++j, ++q) {
-            if (q % NCW != warp) continue;
+        uint16_t* hdst = (shared ? p.hs : p.hr) + (size_t)pbase * inter;
+        for (int j = j0; j < ch.n; j += NCW) {
+            // column of this row in the activation rows (routed rows of
+            // MXFP4 / FP8 layers are stored swizzled)
+            const int e = ch.r0 + j;
+            const int col = shared ? e : 8 * swz_vec(e >> 3, kXM<WFMT>) + (e & 7);
             int q0 = 0;
             for (; q0 + 2 <= npairs; q0 += 2) {
                 const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
@@ -798,7 +828,7 @@ struct Consumer {
                     g[1] *= plan->x_inv[tb], u[1] *= plan->x_inv[tb];
                 }
                 if (lane < 2)
-                    hdst[(size_t)(q0 + lane) * inter + j] =
+                    hdst[(size_t)(q0 + lane) * inter + col] =
                         f32_to_bf16_bits(silu_mul(lane ? g[1] : g[0], lane ? u[1] : u[0]));
             }
             if (q0 < npairs) {
@@ -808,7 +838,7 @@ struct Consumer {
                 g[0] = warp_sum(g[0]);
                 u[0] = warp_sum(u[0]);
                 if (WFMT == 1) g[0] *= plan->x_inv[ta], u[0] *= plan->x_inv[ta];
-                if (lane == 0) hdst[(size_t)q0 * inter + j] = f32_to_bf16_bits(silu_mul(g[0], u[0]));
+                if (lane == 0) hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(g[0], u[0]));
             }
         }
     }
@@ -1232,7 +1262,7 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
                 v.y = f32_to_bf16_bits(f[2]) | ((uint32_t)f32_to_bf16_bits(f[3]) << 16);
                 v.z = f32_to_bf16_bits(f[4]) | ((uint32_t)f32_to_bf16_bits(f[5]) << 16);
                 v.w = f32_to_bf16_bits(f[6]) | ((uint32_t)f32_to_bf16_bits(f[7]) << 16);
-                dst[(size_t)t * nvt + i] = v;
+                dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
             }
             continue;
         }
@@ -1255,7 +1285,7 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
             v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
             v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
             v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
-            dst[(size_t)t * nvt + i] = v;
+            dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
         }
         if (lane == 0) x_inv[t] = exp2i(-sh);
     }
@@ -1369,8 +1399,14 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             if (IO) {
                 load_tokens<WFMT>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.eps, dst,
                                   plan->x_inv, warp, lane, NCW);
-            } else if (WFMT != 1) {
+            } else if (WFMT == 0) {
                 for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+            } else if (WFMT == 2) {
+                const int nvt = p.H / 8;
+                for (int i = tid; i < nv; i += NCT) {
+                    const int v = i % nvt;
+                    dst[i - v + swz_vec(v, kXM<WFMT>)] = __ldg(src + i);
+                }
             } else {
                 // MXFP4 layers hold the tokens in f16 times 2^s_t, s_t chosen
                 // from the token's largest magnitude (exact for bf16 values
@@ -1396,7 +1432,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                         v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
                         v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
                         v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
-                        dst[(size_t)t * nvt + i] = v;
+                        dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
                     }
                     if (lane == 0) plan->x_inv[t] = exp2i(-sh);
                 }
@@ -1432,7 +1468,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             }
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
-            cs.q = 0;
+            cs.qm = 0;
             if (ok) ok = cs.consume_phase();  // shared, then routed gate/up
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
