@@ -409,8 +409,10 @@ struct Producer {
 // Dot products over rows held in shared memory. Lanes stride the row's
 // 16-byte vectors; each token keeps four independent partial sums so that the
 // FMA dependency chains stay short and the loads of several vectors are in
-// flight at once. Token groups are at most two wide (NT), which keeps all
-// accumulators in registers.
+// flight at once. The bf16 products go through the paired fp32 FMA: partial
+// sums (even, odd) of a pair are the two halves of one fma.rn.f32x2, each
+// rounded as a scalar fma would be. Token groups are at most two wide (NT),
+// which keeps all accumulators in registers.
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -418,47 +420,46 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// (p0 + p1) + (p2 + p3) of the four partial sums held as two pairs.
 template <int NT>
-__device__ __forceinline__ void sum4(const float (&pa)[NT][4], float (&acc)[NT]) {
+__device__ __forceinline__ void sum4(const float2 (&pa)[NT][2], float (&acc)[NT]) {
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0] + pa[t][1]) + (pa[t][2] + pa[t][3]);
+    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0].x + pa[t][0].y) + (pa[t][1].x + pa[t][1].y);
 }
 
-// Eight activations of one 16-byte vector as fp32: bf16, or (XH) f16.
+// Eight activations of one 16-byte vector as four fp32 pairs: bf16, or (XH)
+// f16.
 template <bool XH>
-__device__ __forceinline__ void unpack8x(const uint4 v, float (&f)[8]) {
+__device__ __forceinline__ void unpack8x2x(const uint4 v, float2 (&f)[4]) {
     if (XH) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 a = f16x2_to_f32(w[j]);
-            f[2 * j] = a.x;
-            f[2 * j + 1] = a.y;
-        }
+        f[0] = f16x2_to_f32(v.x);
+        f[1] = f16x2_to_f32(v.y);
+        f[2] = f16x2_to_f32(v.z);
+        f[3] = f16x2_to_f32(v.w);
     } else {
-        unpack8(v, f);
+        unpack8x2(v, f);
     }
 }
 
 // acc[t] = row . x_t (bf16 weights, bf16 or (XH) f16 activations, fp32
 // accumulate) over nvec 16-byte vectors; this lane takes vectors lane,
-// lane + STRIDE, ...
+// lane + STRIDE, ... Element e of a vector goes to partial sum e mod 4.
 template <int NT, int STRIDE = 32, bool XH = false, int XM = 0>
 __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                          const uint4* __restrict__ x1, int nvec, int lane, float (&acc)[NT]) {
-    float pa[NT][4];
+    float2 pa[NT][2];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
+    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int v = lane; v < nvec; v += STRIDE) {
-        float fw[8];
-        unpack8(row[v], fw);
+        float2 fw[4];
+        unpack8x2(row[v], fw);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            float fx[8];
-            unpack8x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
+            float2 fx[4];
+            unpack8x2x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
+            for (int e = 0; e < 4; ++e) pa[t][e & 1] = ffma2(fw[e], fx[e], pa[t][e & 1]);
         }
     }
     sum4<NT>(pa, acc);
@@ -469,22 +470,22 @@ template <int NT, bool XH = false, int XM = 0>
 __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const uint4* __restrict__ r3,
                                           const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nvec,
                                           int lane, float (&g)[NT], float (&u)[NT]) {
-    float pg[NT][4], pu[NT][4];
+    float2 pg[NT][2], pu[NT][2];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) pg[t][0] = pg[t][1] = pg[t][2] = pg[t][3] = pu[t][0] = pu[t][1] = pu[t][2] = pu[t][3] = 0.f;
+    for (int t = 0; t < NT; ++t) pg[t][0] = pg[t][1] = pu[t][0] = pu[t][1] = make_float2(0.f, 0.f);
 #pragma unroll 5
     for (int v = lane; v < nvec; v += 32) {
-        float f1[8], f3[8];
-        unpack8(r1[v], f1);
-        unpack8(r3[v], f3);
+        float2 f1[4], f3[4];
+        unpack8x2(r1[v], f1);
+        unpack8x2(r3[v], f3);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            float fx[8];
-            unpack8x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
+            float2 fx[4];
+            unpack8x2x<XH>((t == 0 ? x0 : x1)[swz_vec(v, XM)], fx);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                pg[t][e & 3] = fmaf(f1[e], fx[e], pg[t][e & 3]);
-                pu[t][e & 3] = fmaf(f3[e], fx[e], pu[t][e & 3]);
+            for (int e = 0; e < 4; ++e) {
+                pg[t][e & 1] = ffma2(f1[e], fx[e], pg[t][e & 1]);
+                pu[t][e & 1] = ffma2(f3[e], fx[e], pu[t][e & 1]);
             }
         }
     }
@@ -494,34 +495,35 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
 
 // Four rows (row0 + j * rstride, j < 4) against NT vectors at once: the four
 // rows' loads and FMA chains are independent, so one warp keeps several
-// rows in flight instead of finishing them one after another.
+// rows in flight instead of finishing them one after another. Each row and
+// token keeps two partial sums (even and odd elements).
 template <int NT>
 __device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rstride, const uint4* __restrict__ h0,
                                           const uint4* __restrict__ h1, int nvec, int lane, float (&acc)[4][NT]) {
-    float pa[4][NT][2];
+    float2 pa[4][NT];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) pa[j][t][0] = pa[j][t][1] = 0.f;
+        for (int t = 0; t < NT; ++t) pa[j][t] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
-        float fh[NT][8];
+        float2 fh[NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) unpack8((t == 0 ? h0 : h1)[v], fh[t]);
+        for (int t = 0; t < NT; ++t) unpack8x2((t == 0 ? h0 : h1)[v], fh[t]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float fw[8];
-            unpack8(row0[j * rstride + v], fw);
+            float2 fw[4];
+            unpack8x2(row0[j * rstride + v], fw);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) pa[j][t][e & 1] = fmaf(fw[e], fh[t][e], pa[j][t][e & 1]);
+                for (int e = 0; e < 4; ++e) pa[j][t] = ffma2(fw[e], fh[t][e], pa[j][t]);
         }
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) acc[j][t] = pa[j][t][0] + pa[j][t][1];
+        for (int t = 0; t < NT; ++t) acc[j][t] = pa[j][t].x + pa[j][t].y;
 }
 
 // ---- MXFP4 with f16 block sums. The codes of a 32-element block become

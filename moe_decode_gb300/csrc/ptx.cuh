@@ -140,6 +140,20 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
     f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
 }
 
+// The same eight values as four (even, odd) pairs, the operand shape of the
+// paired fp32 FMA.
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+    return make_float2(bf16lo(w), bf16hi(w));
+}
+__device__ __forceinline__ void unpack8x2(const uint4 v, float2 (&f)[4]) {
+    f[0] = bf16x2_to_f32x2(v.x);
+    f[1] = bf16x2_to_f32x2(v.y);
+    f[2] = bf16x2_to_f32x2(v.z);
+    f[3] = bf16x2_to_f32x2(v.w);
+}
+// d = a * b + c on both halves, each rounded once (fma.rn.f32x2).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     __nv_bfloat16 b = __float2bfloat16_rn(f);
     return *reinterpret_cast<uint16_t*>(&b);
