@@ -641,7 +641,8 @@ __device__ __forceinline__ void dot4_mxh(const uint8_t* const (&crow)[4], const 
 }
 
 // ---- FP8 e4m3 with one fp32 scale per 128 elements of a row: codes
-// decoded to fp32 by the hardware conversion, products in fp32; each 16-code
+// decoded to fp32 by the hardware conversion, products in fp32 through the
+// paired FMA (even and odd partial sums of each 8-code half); each 16-code
 // vector's partial sum is scaled by its block's scale.
 
 // FP8 gate and up rows (codes c1, c3; scales s1, s3 per 128 elements)
@@ -655,27 +656,29 @@ __device__ __forceinline__ void dot2_fp8(const uint4* __restrict__ c1, const flo
     for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
 #pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
-        float f1[16], f3[16];
-        unpack16_e4m3(c1[v], f1);
-        unpack16_e4m3(c3[v], f3);
+        float2 f1[8], f3[8];
+        unpack16_e4m3x2(c1[v], f1);
+        unpack16_e4m3x2(c3[v], f3);
         const float sc1 = s1[v >> 3], sc3 = s3[v >> 3];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const uint4* xt = t == 0 ? x0 : x1;
             const int r = (v >> 2) & 1;  // the vector pair's swizzle (kXM<2>)
-            float fa[8], fb[8];
-            unpack8(xt[2 * v + r], fa);
-            unpack8(xt[2 * v + (1 ^ r)], fb);
-            float pg0 = 0.f, pg1 = 0.f, pu0 = 0.f, pu1 = 0.f;
+            float2 fa[4], fb[4];
+            unpack8x2(xt[2 * v + r], fa);
+            unpack8x2(xt[2 * v + (1 ^ r)], fb);
+            // (even, odd) partial sums of each half of the 16-code vector
+            float2 pg[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 pu[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                pg0 = fmaf(f1[e], fa[e], pg0);
-                pg1 = fmaf(f1[8 + e], fb[e], pg1);
-                pu0 = fmaf(f3[e], fa[e], pu0);
-                pu1 = fmaf(f3[8 + e], fb[e], pu1);
+            for (int e = 0; e < 4; ++e) {
+                pg[0] = ffma2(f1[e], fa[e], pg[0]);
+                pg[1] = ffma2(f1[4 + e], fb[e], pg[1]);
+                pu[0] = ffma2(f3[e], fa[e], pu[0]);
+                pu[1] = ffma2(f3[4 + e], fb[e], pu[1]);
             }
-            g[t] = fmaf(pg0 + pg1, sc1, g[t]);
-            u[t] = fmaf(pu0 + pu1, sc3, u[t]);
+            g[t] = fmaf((pg[0].x + pg[0].y) + (pg[1].x + pg[1].y), sc1, g[t]);
+            u[t] = fmaf((pu[0].x + pu[0].y) + (pu[1].x + pu[1].y), sc3, u[t]);
         }
     }
 }
@@ -691,31 +694,31 @@ __device__ __forceinline__ void dot4_fp8(const uint8_t* const (&crow)[4], const 
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[j][t] = 0.f;
     for (int v = lane; v < nvec; v += 32) {
-        float fh[NT][16];
+        float2 fh[NT][8];
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const uint4* ht = t == 0 ? h0 : h1;
             const int r = (v >> 2) & 1;  // the vector pair's swizzle (kXM<2>)
-            float a8[8], b8[8];
-            unpack8(ht[2 * v + r], a8);
-            unpack8(ht[2 * v + (1 ^ r)], b8);
+            float2 a4[4], b4[4];
+            unpack8x2(ht[2 * v + r], a4);
+            unpack8x2(ht[2 * v + (1 ^ r)], b4);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) fh[t][e] = a8[e], fh[t][8 + e] = b8[e];
+            for (int e = 0; e < 4; ++e) fh[t][e] = a4[e], fh[t][4 + e] = b4[e];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float fw[16];
-            unpack16_e4m3(reinterpret_cast<const uint4*>(crow[j])[v], fw);
+            float2 fw[8];
+            unpack16_e4m3x2(reinterpret_cast<const uint4*>(crow[j])[v], fw);
             const float sc = reinterpret_cast<const float*>(srow[j])[v >> 3];
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float q0 = 0.f, q1 = 0.f;
+                float2 q[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    q0 = fmaf(fw[e], fh[t][e], q0);
-                    q1 = fmaf(fw[8 + e], fh[t][8 + e], q1);
+                for (int e = 0; e < 4; ++e) {
+                    q[0] = ffma2(fw[e], fh[t][e], q[0]);
+                    q[1] = ffma2(fw[4 + e], fh[t][4 + e], q[1]);
                 }
-                acc[j][t] = fmaf(q0 + q1, sc, acc[j][t]);
+                acc[j][t] = fmaf((q[0].x + q[0].y) + (q[1].x + q[1].y), sc, acc[j][t]);
             }
         }
     }

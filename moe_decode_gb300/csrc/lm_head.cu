@@ -55,45 +55,47 @@ __device__ __forceinline__ float lm_warp_sum(float v) {
 template <int WT, int NT>
 __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                        const uint4* __restrict__ x1, int H, int lane, float (&acc)[NT]) {
-    float pa[NT][4];
+    // partial sums p0..p3 (element e to p[e mod 4]) held as two (even, odd)
+    // pairs, each pair one paired fp32 FMA
+    float2 pa[NT][2];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = pa[t][2] = pa[t][3] = 0.f;
+    for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = make_float2(0.f, 0.f);
     if (WT == 0) {
         const int nvec = H / 8;
 #pragma unroll 4
         for (int v = lane; v < nvec; v += 32) {
-            float fw[8];
-            unpack8(row[v], fw);
+            float2 fw[4];
+            unpack8x2(row[v], fw);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float fx[8];
-                unpack8((t == 0 ? x0 : x1)[v], fx);
+                float2 fx[4];
+                unpack8x2((t == 0 ? x0 : x1)[v], fx);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) pa[t][e & 3] = fmaf(fw[e], fx[e], pa[t][e & 3]);
+                for (int e = 0; e < 4; ++e) pa[t][e & 1] = ffma2(fw[e], fx[e], pa[t][e & 1]);
             }
         }
     } else {
         const int nvec = H / 16;
 #pragma unroll 2
         for (int v = lane; v < nvec; v += 32) {
-            float fw[16];
-            unpack16_e4m3(row[v], fw);
+            float2 fw[8];
+            unpack16_e4m3x2(row[v], fw);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
                 const uint4* xt = t == 0 ? x0 : x1;
-                float fa[8], fb[8];
-                unpack8(xt[2 * v], fa);
-                unpack8(xt[2 * v + 1], fb);
+                float2 fa[4], fb[4];
+                unpack8x2(xt[2 * v], fa);
+                unpack8x2(xt[2 * v + 1], fb);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    pa[t][e & 3] = fmaf(fw[e], fa[e], pa[t][e & 3]);
-                    pa[t][e & 3] = fmaf(fw[8 + e], fb[e], pa[t][e & 3]);
+                for (int e = 0; e < 4; ++e) {
+                    pa[t][e & 1] = ffma2(fw[e], fa[e], pa[t][e & 1]);
+                    pa[t][e & 1] = ffma2(fw[4 + e], fb[e], pa[t][e & 1]);
                 }
             }
         }
     }
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0] + pa[t][1]) + (pa[t][2] + pa[t][3]);
+    for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0].x + pa[t][0].y) + (pa[t][1].x + pa[t][1].y);
 }
 
 template <int WT>

@@ -222,6 +222,18 @@ __device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
     }
 }
 
+// The same sixteen values as eight (even, odd) pairs.
+__device__ __forceinline__ void unpack16_e4m3x2(const uint4 c, float2 (&f)[8]) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint32_t lo, hi;
+        e4m3x4_to_f16x2(w[k], lo, hi);
+        f[2 * k] = f16x2_to_f32(lo);
+        f[2 * k + 1] = f16x2_to_f32(hi);
+    }
+}
+
 // 2^(s-127) for an e8m0 byte s (s = 0 is the subnormal 2^-127; s = 255 NaN).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
     if (s == 255u) return __uint_as_float(0x7fc00000u);
