@@ -493,13 +493,18 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
     sum4<NT>(pu, u);
 }
 
-// Four rows (row0 + j * rstride, j < 4) against NT vectors at once: the four
-// rows' loads and FMA chains are independent, so one warp keeps several
-// rows in flight instead of finishing them one after another. Each row and
-// token keeps two partial sums (even and odd elements).
+// Four rows (row0 + min(j, nrow - 1) * rstride, j < 4: rows past nrow repeat
+// the last one and their results are dropped) against NT vectors at once:
+// the four rows' loads and FMA chains are independent, so one warp keeps
+// several rows in flight instead of finishing them one after another. Each
+// row and token keeps two partial sums (even and odd elements).
 template <int NT>
-__device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rstride, const uint4* __restrict__ h0,
-                                          const uint4* __restrict__ h1, int nvec, int lane, float (&acc)[4][NT]) {
+__device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rstride, int nrow,
+                                          const uint4* __restrict__ h0, const uint4* __restrict__ h1, int nvec,
+                                          int lane, float (&acc)[4][NT]) {
+    const uint4* rows[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rows[j] = row0 + min(j, nrow - 1) * rstride;
     float2 pa[4][NT];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -513,7 +518,7 @@ __device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rs
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             float2 fw[4];
-            unpack8x2(row0[j * rstride + v], fw);
+            unpack8x2(rows[j][v], fw);
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -739,8 +744,6 @@ struct Consumer {
     int qm;              // rows go round-robin over the warps, continuing
                          // across chunks: the running row count mod NCW
     int h0;              // first output row of this CTA
-    int c3;              // down chunks seen so far
-    int dg;              // parts a down chunk is split into
 
     __device__ __forceinline__ bool wait_full() { return mbar_wait(ring.full(), ring.ph, p, plan); }
     __device__ __forceinline__ void release() {
@@ -849,16 +852,15 @@ struct Consumer {
     }
 
     // Down projection. A down chunk (one slot, a pair group, a block of
-    // output rows) is split into DG parts of consecutive rows, and part j of
-    // the c-th down chunk goes to warp (c * DG + j) % NCW, so the chunks that
-    // are resident together are worked on by different warps at the same
-    // time. Each (pair, row) result is written exactly once, unweighted, into
-    // ypair; the weighted combine runs after the last chunk, in pair order.
+    // output rows) is split into parts of four consecutive rows; parts go
+    // round-robin over the warps, continuing from chunk to chunk, so that the
+    // chunks resident together are worked on by all warps at once. Each
+    // (pair, row) result is written exactly once, unweighted, into ypair; the
+    // weighted combine runs after the last chunk, in pair order.
     __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
-        const int DG = dg;
-        const int c = c3++;
-        // this warp's parts are j with (c * DG + j) % NCW == warp
-        if ((uint32_t)((warp - (c * DG) % NCW + NCW) % NCW) >= (uint32_t)DG) return;
+        const int nparts = (ch.n + 3) >> 2;
+        const int part0 = claim_rows(nparts);
+        if (part0 >= nparts) return;
         const bool shared = ch.slot < 0;
         const int gbase = (shared ? 0 : p.M + plan->slot_p0[ch.slot]) + ch.p0;  // pair index of q0 = 0
         size_t sofs = 0;
@@ -867,124 +869,93 @@ struct Consumer {
             sofs = s0 - (s0 & ~(size_t)15);
         }
         const int inter = shared ? p.Is : p.I;
-        for (int part = 0; part < DG; ++part) {
-            if ((c * DG + part) % NCW != warp) continue;
-            const int ra = ch.r0 + part * ch.n / DG, rb = ch.r0 + (part + 1) * ch.n / DG;
+        for (int part = part0; part < nparts; part += NCW) {
+            const int r = ch.r0 + 4 * part;
+            const int nrow = min(4, ch.r0 + ch.n - r);
+            float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
             if (WFMT == 0 || shared) {
                 const size_t hb = (size_t)ch.np * inter * 2;
                 const int rstride = inter / 8;  // uint4 per row
-                for (int r = ra; r < rb; r += 4) {
-                    const int nrow = min(4, rb - r);
-                    const uint4* row0 = reinterpret_cast<const uint4*>(st + hb + (size_t)(r - ch.r0) * inter * 2);
-                    float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
-                    int q0 = 0;
-                    for (; q0 + 2 <= ch.np; q0 += 2) {
-                        float acc[4][2];
-                        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
-                        if (nrow == 4) {
-                            dot4_bf16<2>(row0, rstride, ha, ha + rstride, rstride, lane, acc);
-                        } else {  // a partial block: the valid rows one at a time
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] = acc[jj][1] = 0.f;
-                            for (int jj = 0; jj < nrow; ++jj) {
-                                float a1[2];
-                                dot_bf16<2>(row0 + jj * rstride, ha, ha + rstride, rstride, lane, a1);
-                                acc[jj][0] = a1[0];
-                                acc[jj][1] = a1[1];
-                            }
-                        }
-#pragma unroll
-                        for (int o = 16; o; o >>= 1)
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) {
-                                acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
-                                acc[jj][1] += __shfl_xor_sync(0xffffffffu, acc[jj][1], o);
-                            }
-                        if (lane == 0)
-                            for (int jj = 0; jj < nrow; ++jj) {
-                                out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
-                                out[(size_t)(q0 + 1) * p.rpc + jj] = acc[jj][1];
-                            }
+                const uint4* row0 = reinterpret_cast<const uint4*>(st + hb + (size_t)(r - ch.r0) * inter * 2);
+                int q0 = 0;
+                for (; q0 + 2 <= ch.np; q0 += 2) {
+                    float acc[4][2];
+                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
+                    if (nrow > 1) {
+                        dot4_bf16<2>(row0, rstride, nrow, ha, ha + rstride, rstride, lane, acc);
+                    } else {
+                        float a1[2];
+                        dot_bf16<2>(row0, ha, ha + rstride, rstride, lane, a1);
+                        acc[0][0] = a1[0];
+                        acc[0][1] = a1[1];
                     }
-                    if (q0 < ch.np) {
-                        float acc[4][1];
-                        const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
-                        if (nrow == 4) {
-                            dot4_bf16<1>(row0, rstride, ha, ha, rstride, lane, acc);
-                        } else {
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] = 0.f;
-                            for (int jj = 0; jj < nrow; ++jj) {
-                                float a1[1];
-                                dot_bf16<1>(row0 + jj * rstride, ha, ha, rstride, lane, a1);
-                                acc[jj][0] = a1[0];
-                            }
-                        }
-#pragma unroll
-                        for (int o = 16; o; o >>= 1)
-#pragma unroll
-                            for (int jj = 0; jj < 4; ++jj) acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
-                        if (lane == 0)
-                            for (int jj = 0; jj < nrow; ++jj) out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
+                    reduce_store<2>(acc, nrow, out + (size_t)q0 * p.rpc);
+                }
+                if (q0 < ch.np) {
+                    float acc[4][1];
+                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * inter * 2);
+                    if (nrow > 1) {
+                        dot4_bf16<1>(row0, rstride, nrow, ha, ha, rstride, lane, acc);
+                    } else {
+                        float a1[1];
+                        dot_bf16<1>(row0, ha, ha, rstride, lane, a1);
+                        acc[0][0] = a1[0];
                     }
+                    reduce_store<1>(acc, nrow, out + (size_t)q0 * p.rpc);
                 }
                 continue;
             }
-            // MXFP4 / FP8 routed rows, four at a time (rows past the part's
-            // end repeat its last row; their results are dropped)
+            // MXFP4 / FP8 routed rows (rows past the part's end repeat its
+            // last row; their results are dropped)
             constexpr int CD = WFMT == 1 ? 2 : 1;
             const size_t hbytes = (size_t)ch.np * p.I * 2;
             const uint8_t* codes = st + hbytes;
             const uint8_t* scls = st + hbytes + (size_t)ch.n * (p.I / CD) + sofs;
             const int nblk = p.I / 32;
-            for (int r = ra; r < rb; r += 4) {
-                const int nrow = min(4, rb - r);
-                const uint8_t* crow[4];
-                const uint8_t* srow[4];
+            const uint8_t* crow[4];
+            const uint8_t* srow[4];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int j = r - ch.r0 + min(jj, nrow - 1);
-                    crow[jj] = codes + (size_t)j * (p.I / CD);
-                    srow[jj] = scls + (size_t)j * nblk;
-                }
-                float* out = ypair + (size_t)gbase * p.rpc + (r - h0);
-                int q0 = 0;
-                for (; q0 + 2 <= ch.np; q0 += 2) {
-                    float acc[4][2];
-                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
-                    if (WFMT == 1)
-                        dot4_mxh<2>(crow, srow, ha, ha + p.I / 8, nblk, lane, acc);
-                    else
-                        dot4_fp8<2>(crow, srow, ha, ha + p.I / 8, p.I / 16, lane, acc);
-#pragma unroll
-                    for (int o = 16; o; o >>= 1)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
-                            acc[jj][1] += __shfl_xor_sync(0xffffffffu, acc[jj][1], o);
-                        }
-                    if (lane == 0)
-                        for (int jj = 0; jj < nrow; ++jj) {
-                            out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
-                            out[(size_t)(q0 + 1) * p.rpc + jj] = acc[jj][1];
-                        }
-                }
-                if (q0 < ch.np) {
-                    float acc[4][1];
-                    const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
-                    if (WFMT == 1)
-                        dot4_mxh<1>(crow, srow, ha, ha, nblk, lane, acc);
-                    else
-                        dot4_fp8<1>(crow, srow, ha, ha, p.I / 16, lane, acc);
-#pragma unroll
-                    for (int o = 16; o; o >>= 1)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) acc[jj][0] += __shfl_xor_sync(0xffffffffu, acc[jj][0], o);
-                    if (lane == 0)
-                        for (int jj = 0; jj < nrow; ++jj) out[(size_t)q0 * p.rpc + jj] = acc[jj][0];
-                }
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = r - ch.r0 + min(jj, nrow - 1);
+                crow[jj] = codes + (size_t)j * (p.I / CD);
+                srow[jj] = scls + (size_t)j * nblk;
+            }
+            int q0 = 0;
+            for (; q0 + 2 <= ch.np; q0 += 2) {
+                float acc[4][2];
+                const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
+                if (WFMT == 1)
+                    dot4_mxh<2>(crow, srow, ha, ha + p.I / 8, nblk, lane, acc);
+                else
+                    dot4_fp8<2>(crow, srow, ha, ha + p.I / 8, p.I / 16, lane, acc);
+                reduce_store<2>(acc, nrow, out + (size_t)q0 * p.rpc);
+            }
+            if (q0 < ch.np) {
+                float acc[4][1];
+                const uint4* ha = reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2);
+                if (WFMT == 1)
+                    dot4_mxh<1>(crow, srow, ha, ha, nblk, lane, acc);
+                else
+                    dot4_fp8<1>(crow, srow, ha, ha, p.I / 16, lane, acc);
+                reduce_store<1>(acc, nrow, out + (size_t)q0 * p.rpc);
             }
         }
+    }
+
+    // Warp sums of a four-row group's lane partials; lane 0 stores the
+    // first nrow rows for each of the NT pairs (pair stride rpc).
+    template <int NT>
+    __device__ __forceinline__ void reduce_store(float (&acc)[4][NT], int nrow, float* out) const {
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) acc[jj][t] += __shfl_xor_sync(0xffffffffu, acc[jj][t], o);
+        if (lane == 0)
+            for (int jj = 0; jj < nrow; ++jj)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) out[(size_t)t * p.rpc + jj] = acc[jj][t];
     }
 
     // Consumes the chunks of one phase, up to its end marker: waits for each
@@ -1394,7 +1365,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         // ---------------- consumers
         const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
-        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0, 0, (NCW + p.ns - 1) / p.ns};
+        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0};
         pdl_wait();
         if (tid == 0) plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
         {
