@@ -409,9 +409,12 @@ struct Producer {
 // Dot products over rows held in shared memory. Lanes stride the row's
 // 16-byte vectors; each token keeps four independent partial sums so that the
 // FMA dependency chains stay short and the loads of several vectors are in
-// flight at once. The bf16 products go through the paired fp32 FMA: partial
-// sums (even, odd) of a pair are the two halves of one fma.rn.f32x2, each
-// rounded as a scalar fma would be. Token groups are at most two wide (NT),
+// flight at once. bf16 x bf16 products go through the mixed-precision fma
+// (fma.rn.f32.bf16: bf16 operands straight from the packed registers, fp32
+// addend, one rounding), which needs no unpacking; with f16 tokens (MXFP4
+// layers) the weights are unpacked to fp32 pairs and go through the paired
+// fp32 FMA (fma.rn.f32x2). Either way each partial sum is rounded as a
+// scalar fp32 fma would round it. Token groups are at most two wide (NT),
 // which keeps all accumulators in registers.
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -452,6 +455,18 @@ __device__ __forceinline__ void dot_bf16(const uint4* __restrict__ row, const ui
     for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = make_float2(0.f, 0.f);
 #pragma unroll 4
     for (int v = lane; v < nvec; v += STRIDE) {
+        if (!XH) {
+            const uint4 w = row[v];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4 x = (t == 0 ? x0 : x1)[swz_vec(v, XM)];
+                const uint32_t xx[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) fma_bf16x2(ww[e], xx[e], pa[t][e & 1].x, pa[t][e & 1].y);
+            }
+            continue;
+        }
         float2 fw[4];
         unpack8x2(row[v], fw);
 #pragma unroll
@@ -475,6 +490,21 @@ __device__ __forceinline__ void dot2_bf16(const uint4* __restrict__ r1, const ui
     for (int t = 0; t < NT; ++t) pg[t][0] = pg[t][1] = pu[t][0] = pu[t][1] = make_float2(0.f, 0.f);
 #pragma unroll 5
     for (int v = lane; v < nvec; v += 32) {
+        if (!XH) {
+            const uint4 a = r1[v], b = r3[v];
+            const uint32_t w1[4] = {a.x, a.y, a.z, a.w}, w3[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint4 x = (t == 0 ? x0 : x1)[swz_vec(v, XM)];
+                const uint32_t xx[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    fma_bf16x2(w1[e], xx[e], pg[t][e & 1].x, pg[t][e & 1].y);
+                    fma_bf16x2(w3[e], xx[e], pu[t][e & 1].x, pu[t][e & 1].y);
+                }
+            }
+            continue;
+        }
         float2 f1[4], f3[4];
         unpack8x2(r1[v], f1);
         unpack8x2(r3[v], f3);
@@ -512,17 +542,20 @@ __device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rs
         for (int t = 0; t < NT; ++t) pa[j][t] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
-        float2 fh[NT][4];
+        uint32_t hh[NT][4];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) unpack8x2((t == 0 ? h0 : h1)[v], fh[t]);
+        for (int t = 0; t < NT; ++t) {
+            const uint4 h = (t == 0 ? h0 : h1)[v];
+            hh[t][0] = h.x, hh[t][1] = h.y, hh[t][2] = h.z, hh[t][3] = h.w;
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float2 fw[4];
-            unpack8x2(rows[j][v], fw);
+            const uint4 w = rows[j][v];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pa[j][t] = ffma2(fw[e], fh[t][e], pa[j][t]);
+                for (int e = 0; e < 4; ++e) fma_bf16x2(ww[e], hh[t][e], pa[j][t].x, pa[j][t].y);
         }
     }
 #pragma unroll

@@ -56,7 +56,8 @@ template <int WT, int NT>
 __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                        const uint4* __restrict__ x1, int H, int lane, float (&acc)[NT]) {
     // partial sums p0..p3 (element e to p[e mod 4]) held as two (even, odd)
-    // pairs, each pair one paired fp32 FMA
+    // pairs: bf16 rows through the mixed-precision fma (bf16 operands, fp32
+    // addend), e4m3 rows decoded to fp32 pairs and the paired fp32 FMA
     float2 pa[NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = make_float2(0.f, 0.f);
@@ -64,14 +65,14 @@ __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint
         const int nvec = H / 8;
 #pragma unroll 4
         for (int v = lane; v < nvec; v += 32) {
-            float2 fw[4];
-            unpack8x2(row[v], fw);
+            const uint4 w = row[v];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                float2 fx[4];
-                unpack8x2((t == 0 ? x0 : x1)[v], fx);
+                const uint4 x = (t == 0 ? x0 : x1)[v];
+                const uint32_t xx[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) pa[t][e & 1] = ffma2(fw[e], fx[e], pa[t][e & 1]);
+                for (int e = 0; e < 4; ++e) fma_bf16x2(ww[e], xx[e], pa[t][e & 1].x, pa[t][e & 1].y);
             }
         }
     } else {

@@ -151,6 +151,14 @@ __device__ __forceinline__ void unpack8x2(const uint4 v, float2 (&f)[4]) {
     f[2] = bf16x2_to_f32x2(v.z);
     f[3] = bf16x2_to_f32x2(v.w);
 }
+// lo += w.lo * x.lo, hi += w.hi * x.hi for bf16 pairs w, x, in fp32 with
+// one rounding each (the mixed-precision fma: bf16 operands, fp32 addend).
+__device__ __forceinline__ void fma_bf16x2(uint32_t w, uint32_t x, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w), "r"(x));
+}
 // d = a * b + c on both halves, each rounded once (fma.rn.f32x2).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
