@@ -355,7 +355,9 @@ int moe_lm_head(const void* x, int M, const void* W, const float* w_scale, int V
     p.G = g_opt.grid_ctas > 0 ? g_opt.grid_ctas : dev.sms;
     if (p.G > dev.sms) return MOE_EINVAL;
     p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
-    const size_t bar_bytes = 128, x_bytes = align_up((size_t)M * H * 2, 128);
+    // barriers and the abort flag in the first 128 bytes, per-token scales
+    // (FP8 rows) in the next 128
+    const size_t bar_bytes = 256, x_bytes = align_up((size_t)M * H * 2, 128);
     if ((size_t)dev.smem_optin <= bar_bytes + x_bytes) return MOE_ESHAPE;
     int ns = (int)(((size_t)dev.smem_optin - bar_bytes - x_bytes) / moe::kStageBytes);
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;

@@ -50,14 +50,20 @@ __device__ __forceinline__ float lm_warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float lm_warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
 // acc[t] = row . x_t over H elements; this lane takes 16-byte weight vectors
 // lane, lane + 32, ... (bf16: 8 elements, e4m3: 16 elements per vector).
 template <int WT, int NT>
 __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint4* __restrict__ x0,
                                        const uint4* __restrict__ x1, int H, int lane, float (&acc)[NT]) {
     // partial sums p0..p3 (element e to p[e mod 4]) held as two (even, odd)
-    // pairs: bf16 rows through the mixed-precision fma (bf16 operands, fp32
-    // addend), e4m3 rows decoded to fp32 pairs and the paired fp32 FMA
+    // pairs, each element through the mixed-precision fma (16-bit operands,
+    // fp32 addend, one rounding)
     float2 pa[NT][2];
 #pragma unroll
     for (int t = 0; t < NT; ++t) pa[t][0] = pa[t][1] = make_float2(0.f, 0.f);
@@ -76,21 +82,25 @@ __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint
             }
         }
     } else {
+        // e4m3 codes as f16 pairs against the f16 tokens (held times 2^s_t,
+        // vector pairs swizzled: vector 2v + b of a token row sits at
+        // 2v + (b ^ ((v >> 2) & 1))), through the mixed-precision fma;
+        // every product is exact
         const int nvec = H / 16;
 #pragma unroll 2
         for (int v = lane; v < nvec; v += 32) {
-            float2 fw[8];
-            unpack16_e4m3x2(row[v], fw);
+            uint32_t w[8];
+            e4m3x16_to_f16x2(row[v], w);
+            const int sw = (v >> 2) & 1;
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
                 const uint4* xt = t == 0 ? x0 : x1;
-                float2 fa[4], fb[4];
-                unpack8x2(xt[2 * v], fa);
-                unpack8x2(xt[2 * v + 1], fb);
+                const uint4 xa = xt[2 * v + sw], xb = xt[2 * v + (1 ^ sw)];
+                const uint32_t xx[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    pa[t][e & 1] = ffma2(fw[e], fa[e], pa[t][e & 1]);
-                    pa[t][e & 1] = ffma2(fw[4 + e], fb[e], pa[t][e & 1]);
+                    fma_f16x2(w[e], xx[e], pa[t][e & 1].x, pa[t][e & 1].y);
+                    fma_f16x2(w[4 + e], xx[4 + e], pa[t][e & 1].x, pa[t][e & 1].y);
                 }
             }
         }
@@ -108,6 +118,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t bars = smem_u32(smem + p.off_bar);
     volatile int* flag = reinterpret_cast<volatile int*>(smem + p.off_bar + 2 * p.ns * 8);
+    float* x_inv = reinterpret_cast<float*>(smem + p.off_bar + 128);  // FP8: 2^-s_t per token
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + p.off_x);
     if (tid == 0) {
         for (int i = 0; i < p.ns; ++i) {
@@ -157,19 +168,50 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
-            const int nv = p.M * p.H / 8;
-            for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+            if (WT == 0) {
+                const int nv = p.M * p.H / 8;
+                for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+            } else {
+                // FP8 rows: tokens in f16 times 2^s_t, s_t chosen from the
+                // token's largest magnitude (exact for bf16 values in f16's
+                // normal range), one warp per token
+                const int nvt = p.H / 8;
+                for (int t = warp; t < p.M; t += NCW) {
+                    float mx = 0.f;
+                    for (int i = lane; i < nvt; i += 32) {
+                        float f[8];
+                        unpack8(__ldg(src + (size_t)t * nvt + i), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(f[e]));
+                    }
+                    mx = lm_warp_max(mx);
+                    const int sh = f16_range_shift(mx);
+                    const float sc = exp2i(sh);
+                    for (int i = lane; i < nvt; i += 32) {
+                        float f[8];
+                        unpack8(__ldg(src + (size_t)t * nvt + i), f);
+                        uint4 v;
+                        v.x = f32x2_to_f16x2(f[0] * sc, f[1] * sc);
+                        v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
+                        v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
+                        v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
+                        dst[(size_t)t * nvt + (i ^ ((i >> 3) & 1))] = v;
+                    }
+                    if (lane == 0) x_inv[t] = exp2i(-sh);
+                }
+            }
         }
         named_bar_sync(1, NCT);
         uint32_t s = 0, ph = 0;
-        int q = 0;
+        int qm = 0;  // rows go round-robin over the warps: running row count mod NCW
         const int nvx = p.H / 8;
         for (int r = v0; r < v1; r += cap) {
             const int nr = min(cap, v1 - r);
             if (!lm_wait(bars + s * 8, ph, p, flag)) break;
             const uint8_t* st = reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(base + s * LSB));
-            for (int j = 0; j < nr; ++j, ++q) {
-                if (q % NCW != warp) continue;
+            const int j0 = warp >= qm ? warp - qm : warp - qm + NCW;  // first row of this warp
+            qm = (qm + nr) % NCW;
+            for (int j = j0; j < nr; j += NCW) {
                 const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * rowbytes);
                 const float sc = WT == 0 ? 1.f : __ldg(p.scale + r + j);
                 int t = 0;
@@ -179,6 +221,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
                     lm_dot<WT, 2>(row, xa, xa + nvx, p.H, lane, acc);
                     acc[0] = lm_warp_sum(acc[0]);
                     acc[1] = lm_warp_sum(acc[1]);
+                    if (WT != 0) acc[0] *= x_inv[t], acc[1] *= x_inv[t + 1];
                     if (lane == 0) {
                         p.logits[(size_t)t * p.V + r + j] = acc[0] * sc;
                         p.logits[(size_t)(t + 1) * p.V + r + j] = acc[1] * sc;
@@ -189,6 +232,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
                     const uint4* xa = reinterpret_cast<const uint4*>(xs) + (size_t)t * nvx;
                     lm_dot<WT, 1>(row, xa, xa, p.H, lane, acc);
                     acc[0] = lm_warp_sum(acc[0]);
+                    if (WT != 0) acc[0] *= x_inv[t];
                     if (lane == 0) p.logits[(size_t)t * p.V + r + j] = acc[0] * sc;
                 }
             }

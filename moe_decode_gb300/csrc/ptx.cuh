@@ -159,6 +159,13 @@ __device__ __forceinline__ void fma_bf16x2(uint32_t w, uint32_t x, float& lo, fl
         : "+f"(lo), "+f"(hi)
         : "r"(w), "r"(x));
 }
+// The same with f16 pairs (fma.rn.f32.f16).
+__device__ __forceinline__ void fma_f16x2(uint32_t w, uint32_t x, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, xl, %0;\n\tfma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w), "r"(x));
+}
 // d = a * b + c on both halves, each rounded once (fma.rn.f32x2).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
@@ -228,6 +235,15 @@ __device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
         f[4 * k + 2] = b.x;
         f[4 * k + 3] = b.y;
     }
+}
+
+// Sixteen e4m3 codes (one uint4) as eight f16 pairs: w[j] holds codes 2j
+// (low half) and 2j + 1. Every e4m3 value is exact in f16.
+__device__ __forceinline__ void e4m3x16_to_f16x2(const uint4 c, uint32_t (&w)[8]) {
+    e4m3x4_to_f16x2(c.x, w[0], w[1]);
+    e4m3x4_to_f16x2(c.y, w[2], w[3]);
+    e4m3x4_to_f16x2(c.z, w[4], w[5]);
+    e4m3x4_to_f16x2(c.w, w[6], w[7]);
 }
 
 // The same sixteen values as eight (even, odd) pairs.
