@@ -423,6 +423,33 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Warp sums of two values in one butterfly: at the first level each half of
+// the warp keeps one of them, so lanes 0-15 end with sum(g) and lanes 16-31
+// with sum(u). Every level pairs the same lanes as warp_sum, so each sum is
+// bit-identical to warp_sum's.
+__device__ __forceinline__ float warp_sum2(float g, float u, int lane) {
+    const bool h16 = (lane & 16) != 0;
+    float a = h16 ? u : g;
+    a += __shfl_xor_sync(0xffffffffu, h16 ? g : u, 16);
+#pragma unroll
+    for (int o = 8; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    return a;
+}
+
+// The same for four values: lanes 0-7 end with sum(g0), 8-15 with sum(u0),
+// 16-23 with sum(g1), 24-31 with sum(u1).
+__device__ __forceinline__ float warp_sum4(float g0, float u0, float g1, float u1, int lane) {
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    float kg = h16 ? g1 : g0, ku = h16 ? u1 : u0;
+    kg += __shfl_xor_sync(0xffffffffu, h16 ? g0 : g1, 16);
+    ku += __shfl_xor_sync(0xffffffffu, h16 ? u0 : u1, 16);
+    float a = h8 ? ku : kg;
+    a += __shfl_xor_sync(0xffffffffu, h8 ? kg : ku, 8);
+#pragma unroll
+    for (int o = 4; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    return a;
+}
+
 // (p0 + p1) + (p2 + p3) of the four partial sums held as two pairs.
 template <int NT>
 __device__ __forceinline__ void sum4(const float2 (&pa)[NT][2], float (&acc)[NT]) {
@@ -860,26 +887,28 @@ struct Consumer {
                 const int tb = shared ? q0 + 1 : plan->pair_tok[pbase + q0 + 1];
                 float g[2], u[2];
                 gateup_group<2>(st, ch, j, ta, tb, shared, g, u);
-                g[0] = warp_sum(g[0]);
-                u[0] = warp_sum(u[0]);
-                g[1] = warp_sum(g[1]);
-                u[1] = warp_sum(u[1]);
-                if (WFMT == 1) {  // tokens are held times 2^s_t
-                    g[0] *= plan->x_inv[ta], u[0] *= plan->x_inv[ta];
-                    g[1] *= plan->x_inv[tb], u[1] *= plan->x_inv[tb];
+                // lanes 0 and 16 end with (g, u) of the pair's first and
+                // second token
+                float gs = warp_sum4(g[0], u[0], g[1], u[1], lane);
+                float us = __shfl_down_sync(0xffffffffu, gs, 8);
+                if ((lane & 15) == 0) {
+                    if (WFMT == 1) {  // tokens are held times 2^s_t
+                        const float xi = plan->x_inv[lane ? tb : ta];
+                        gs *= xi, us *= xi;
+                    }
+                    hdst[(size_t)(q0 + (lane >> 4)) * inter + col] = f32_to_bf16_bits(silu_mul(gs, us));
                 }
-                if (lane < 2)
-                    hdst[(size_t)(q0 + lane) * inter + col] =
-                        f32_to_bf16_bits(silu_mul(lane ? g[1] : g[0], lane ? u[1] : u[0]));
             }
             if (q0 < npairs) {
                 const int ta = shared ? q0 : plan->pair_tok[pbase + q0];
                 float g[1], u[1];
                 gateup_group<1>(st, ch, j, ta, ta, shared, g, u);
-                g[0] = warp_sum(g[0]);
-                u[0] = warp_sum(u[0]);
-                if (WFMT == 1) g[0] *= plan->x_inv[ta], u[0] *= plan->x_inv[ta];
-                if (lane == 0) hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(g[0], u[0]));
+                float gs = warp_sum2(g[0], u[0], lane);
+                float us = __shfl_down_sync(0xffffffffu, gs, 16);
+                if (lane == 0) {
+                    if (WFMT == 1) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
+                    hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(gs, us));
+                }
             }
         }
     }
@@ -975,20 +1004,17 @@ struct Consumer {
         }
     }
 
-    // Warp sums of a four-row group's lane partials; lane 0 stores the
-    // first nrow rows for each of the NT pairs (pair stride rpc).
+    // Warp sums of a four-row group's lane partials, four rows per
+    // butterfly (row jj ends in lanes 8 jj .. 8 jj + 7); lane 8 jj stores
+    // row jj, if jj < nrow, for each of the NT pairs (pair stride rpc).
     template <int NT>
     __device__ __forceinline__ void reduce_store(float (&acc)[4][NT], int nrow, float* out) const {
+        const int jj = lane >> 3;
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                for (int t = 0; t < NT; ++t) acc[jj][t] += __shfl_xor_sync(0xffffffffu, acc[jj][t], o);
-        if (lane == 0)
-            for (int jj = 0; jj < nrow; ++jj)
-#pragma unroll
-                for (int t = 0; t < NT; ++t) out[(size_t)t * p.rpc + jj] = acc[jj][t];
+        for (int t = 0; t < NT; ++t) {
+            const float a = warp_sum4(acc[0][t], acc[1][t], acc[2][t], acc[3][t], lane);
+            if ((lane & 7) == 0 && jj < nrow) out[(size_t)t * p.rpc + jj] = a;
+        }
     }
 
     // Consumes the chunks of one phase, up to its end marker: waits for each
