@@ -7,7 +7,9 @@
 namespace moe {
 cudaError_t launch_layer_fp8(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
     const bool io = p.gamma != nullptr || p.residual != 0;
-    return launch_persistent(io ? moe_layer_kernel<2, true> : moe_layer_kernel<2, false>, block_threads(2), p,
-                             stream, pdl, coop);
+    const bool one = p.M == 1 && p.mode == kModeLayer;
+    auto* kernel = io ? (one ? moe_layer_kernel<2, true, true> : moe_layer_kernel<2, true, false>)
+                      : (one ? moe_layer_kernel<2, false, true> : moe_layer_kernel<2, false, false>);
+    return launch_persistent(kernel, block_threads(2), p, stream, pdl, coop);
 }
 }  // namespace moe

@@ -1071,7 +1071,7 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
 template <int EPL, bool VAR>
 __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lrow, const int E, const int k,
                                        int lane, uint32_t tag, const LayerParams& p, Plan* plan,
-                                       int32_t* __restrict__ sel_e, float* __restrict__ sel_w) {
+                                       int32_t* __restrict__ sel_e, float* __restrict__ sel_w, bool publish) {
     float lg[EPL];
     uint64_t t0 = 0;
     for (int spin = 0;; ++spin) {
@@ -1148,7 +1148,13 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
         const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
         const uint32_t we = __reduce_min_sync(0xffffffffu, bk == wk ? bi : 0xffffffffu);
         float ws = 0.f;
-        if (lane == 0) sel_e[jj] = (int32_t)we;
+        if (lane == 0) {
+            sel_e[jj] = (int32_t)we;
+            if (publish) {  // slot jj is the jj-th selected expert: its tiles may stream now
+                plan->slot_e[jj] = (int16_t)we;
+                st_release_cta(&plan->known, jj + 1);
+            }
+        }
         if (we == bi) {  // this lane won: take its score, drop the entry, find the next best
             bk = 0u;
             bi = 0xffffffffu;
@@ -1180,7 +1186,7 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
 }
 
 static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* plan, int warp, int lane,
-                                                   int nwarps) {
+                                                   int nwarps, bool publish) {
     // the debug hook waits for a tag that never comes
     const uint32_t tag = plan->tag + (p.force_timeout ? 1u : 0u);
     for (int t = warp; t < p.M; t += nwarps) {
@@ -1189,12 +1195,13 @@ static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* p
         float* sw = plan->sel_w + t * p.k;
         const bool var = p.scoring != 0 || p.bias != nullptr;
         bool ok;
+        const bool pub = publish && t == 0;
         if (p.E <= 512)
-            ok = var ? topk_warp<16, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw)
-                     : topk_warp<16, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw);
+            ok = var ? topk_warp<16, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub)
+                     : topk_warp<16, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub);
         else
-            ok = var ? topk_warp<32, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw)
-                     : topk_warp<32, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw);
+            ok = var ? topk_warp<32, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub)
+                     : topk_warp<32, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub);
         if (!ok) return;
     }
 }
@@ -1331,29 +1338,57 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
 // producer claims the next chunk from a global counter, so that CTAs that
 // run ahead take more. Two claims are kept in flight to hide the atomic's
 // latency. Which CTA computes a row does not change its result.
+// With one token (incremental plan) the slots are the selected experts in
+// selection order, published one top-k round at a time: a claim waits
+// (bounded) until its slot is known, so the first expert's tiles stream
+// while the top-k is still ranking the others.
 template <int WFMT>
-__device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT>& pr, const LayerParams& p, Plan* plan) {
+__device__ __forceinline__ bool wait_known(const LayerParams& p, Plan* plan, int n) {
+    if (ld_acquire_cta(&plan->known) >= n) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        __nanosleep(32);
+        if (ld_acquire_cta(&plan->known) >= n) return true;
+        if ((spin & 15u) == 0) {
+            if (aborted(plan)) return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                set_abort(p, plan, -101 /* MOE_ETIMEOUT */);
+                return false;
+            }
+        }
+    }
+}
+
+template <int WFMT>
+__device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT>& pr, const LayerParams& p, Plan* plan,
+                                                    bool incremental) {
     const uint32_t cap = (uint32_t)gateup_cap<WFMT>(p, true), I = (uint32_t)p.I;
     const uint32_t cps = (I + cap - 1) / cap;  // chunks per slot
+    if (incremental && !wait_known<WFMT>(p, plan, 1)) return false;
     const uint32_t U = (uint32_t)plan->nslot * cps;
     unsigned* wc = p.ctrl + kCtlWork;
     uint32_t a = atomicAdd(wc, 1u), b = atomicAdd(wc, 1u);
     bool ok = true;
     while (ok && a < U) {
         const uint32_t slot = a / cps, r0 = (a - slot * cps) * cap;
+        if (incremental && !wait_known<WFMT>(p, plan, (int)slot + 1)) return false;
         const Chunk c{1, (int)slot, (int)r0, (int)min(cap, I - r0), 0, 0};
         const uint32_t nxt = atomicAdd(wc, 1u);
         ok = pr.issue(c);
         a = b;
         b = nxt;
     }
+    // the down tiles that follow need every slot's expert
+    if (ok && incremental) ok = wait_known<WFMT>(p, plan, plan->nslot);
     return ok;
 }
 
 // ------------------------------------------------------------ the kernel
 // IO: the input is normalised in the kernel and/or the residual is added
-// (compiled only into the launches that ask for it).
-template <int WFMT, bool IO>
+// (compiled only into the launches that ask for it). ONE: a one-token layer
+// launch (route + FFN, M = 1), whose plan is built incrementally; a separate
+// instantiation, so that the general kernel's code stays as it is.
+template <int WFMT, bool IO, bool ONE>
 __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
     constexpr int NCW = consumer_warps(WFMT);
     constexpr int NCT = NCW * 32;
@@ -1378,6 +1413,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         mbar_init(plan_bar, 1);
         plan->abort = 0;
         plan->npend = 0;
+        plan->known = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -1385,6 +1421,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
 
     const Ring ring0{smem_u32(smem), bars, (uint32_t)p.ns, 0u, 0u, 0u};
     const bool has_route = (p.mode & kModeRoute) != 0, has_ffn = (p.mode & kModeFfn) != 0;
+    // One token: the plan is built incrementally, one slot per top-k round
+    constexpr bool incremental = ONE;
     ChunkGen<WFMT> gen;
     Chunk ch;
 
@@ -1405,9 +1443,9 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             trace_mark(p, 9);
             pdl_wait();
             if (ok && has_ffn) {
-                ok = mbar_wait(plan_bar, 0, p, plan);
+                if (!incremental) ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
-                if (ok) ok = issue_routed_gateup(pr, p, plan);
+                if (ok) ok = issue_routed_gateup(pr, p, plan, incremental);
                 if (ok) ok = pr.issue_end();
                 trace_mark(p, 11);
                 if (ok)
@@ -1481,11 +1519,44 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         named_bar_sync(1, NCT);
         if (tid == 0) trace_mark(p, 1);
         bool ok = true;
-        if (has_route) {
+        if (has_route && incremental) {
+            ok = cs.consume_phase();
+            if (tid == 0) trace_mark(p, 2);
+            // One token: the k selected experts are distinct, and slot s is
+            // the s-th one selected (one pair each). Warp 0 ranks the token
+            // and publishes each slot as its round completes; the producer
+            // starts streaming that expert's gate/up tiles at once. The
+            // other warps go straight on to the ring. The combine still
+            // sums the pairs in ascending expert order (plan->order).
+            if (warp == 0) {
+                for (int i = lane; i <= p.k; i += 32) plan->slot_p0[i] = (int16_t)i;
+                for (int i = lane; i < p.k; i += 32) plan->pair_tok[i] = 0;
+                if (lane == 0) {
+                    plan->nslot = p.k;
+                    plan->npairs = p.k;
+                }
+                __syncwarp();
+                if (!aborted(plan)) topk_tokens(p, plan, warp, lane, 1, true);
+                if (tid == 0) trace_mark(p, 4);
+                __syncwarp();
+                if (lane < p.k && !aborted(plan)) {
+                    const int e = plan->sel_e[lane];
+                    plan->pair_w[lane] = plan->sel_w[lane];
+                    int rk = 0;
+                    for (int j = 0; j < p.k; ++j) rk += plan->sel_e[j] < e;
+                    plan->order[rk] = (int16_t)lane;
+                    if (cta == 0) {
+                        if (p.idx_out) p.idx_out[lane] = e;
+                        if (p.w_out) p.w_out[lane] = plan->sel_w[lane];
+                    }
+                }
+                if (tid == 0) trace_mark(p, 5);
+            }
+        } else if (has_route) {
             ok = cs.consume_phase();
             if (tid == 0) trace_mark(p, 2);
             // no grid barrier: each token's warp waits for the tagged logits
-            if (!aborted(plan)) topk_tokens(p, plan, warp, lane, NCW);
+            if (!aborted(plan)) topk_tokens(p, plan, warp, lane, NCW, false);
             if (tid == 0) trace_mark(p, 4);
             named_bar_sync(1, NCT);
             if (cta == 0 && !aborted(plan)) {
@@ -1496,10 +1567,12 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             }
         }
         if (has_ffn) {
-            build_plan(p, plan, tid, NCT, cta == 0);
-            if (tid == 0) {
-                mbar_arrive(plan_bar);
-                trace_mark(p, 5);
+            if (!incremental) {
+                build_plan(p, plan, tid, NCT, cta == 0);
+                if (tid == 0) {
+                    mbar_arrive(plan_bar);
+                    trace_mark(p, 5);
+                }
             }
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
@@ -1517,13 +1590,21 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             if (!aborted(plan)) {
                 const int nr = h1 - h0;
                 // y[t][r] = shared(t)[r] + sum over routed pairs of token t, in
-                // pair order (experts ascending), of w * down(pair)[r]
+                // ascending expert order, of w * down(pair)[r]
                 const int npr = plan->npairs;
                 for (int i = tid; i < p.M * nr; i += NCT) {
                     const int t = i / nr, r = i - t * nr;
                     float v = p.Is > 0 ? ypair[(size_t)t * p.rpc + r] : 0.f;
-                    for (int q = 0; q < npr; ++q)
-                        if (plan->pair_tok[q] == t) v = fmaf(plan->pair_w[q], ypair[(size_t)(p.M + q) * p.rpc + r], v);
+                    if (incremental) {  // one token: its k pairs, in the published order
+                        for (int qq = 0; qq < npr; ++qq) {
+                            const int q = plan->order[qq];
+                            v = fmaf(plan->pair_w[q], ypair[(size_t)(1 + q) * p.rpc + r], v);
+                        }
+                    } else {  // pairs are grouped by ascending expert
+                        for (int q = 0; q < npr; ++q)
+                            if (plan->pair_tok[q] == t)
+                                v = fmaf(plan->pair_w[q], ypair[(size_t)(p.M + q) * p.rpc + r], v);
+                    }
                     if (IO && p.residual) v += bf16lo(p.x[(size_t)t * p.H + h0 + r]);  // the layer's input
                     p.y[(size_t)t * p.H + h0 + r] = f32_to_bf16_bits(v);
                 }

@@ -8,8 +8,10 @@
 namespace moe {
 cudaError_t launch_layer_mxfp4(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop) {
     const bool io = p.gamma != nullptr || p.residual != 0;
-    return launch_persistent(io ? moe_layer_kernel<1, true> : moe_layer_kernel<1, false>, block_threads(1), p,
-                             stream, pdl, coop);
+    const bool one = p.M == 1 && p.mode == kModeLayer;
+    auto* kernel = io ? (one ? moe_layer_kernel<1, true, true> : moe_layer_kernel<1, true, false>)
+                      : (one ? moe_layer_kernel<1, false, true> : moe_layer_kernel<1, false, false>);
+    return launch_persistent(kernel, block_threads(1), p, stream, pdl, coop);
 }
 
 __global__ void mxfp4_dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,

@@ -91,8 +91,11 @@ struct Plan {
     int32_t first[kMaxEntries];
     int16_t pair_tok[kMaxEntries];  // routed (token, weight) pairs grouped by expert
     float pair_w[kMaxEntries];
-    int16_t slot_e[kMaxEntries];    // distinct routed experts, ascending
+    int16_t slot_e[kMaxEntries];    // distinct routed experts (ascending; at
+                                    // M = 1 in selection order)
     int16_t slot_p0[kMaxEntries + 1];
+    int16_t order[kMaxK];           // M = 1: its pairs by ascending expert (combine order)
+    int32_t known;                  // M = 1: slots whose expert is known so far
     float x_inv[kMaxM];             // MXFP4 layers: tokens are held in f16 times
                                     // 2^s_t; x_inv[t] = 2^-s_t
     int32_t nslot;

@@ -119,6 +119,17 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// Release store / acquire load of a 32-bit word at CTA scope (a flag in
+// shared memory that one warp publishes and another polls).
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+    asm volatile("st.release.cta.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Relaxed GPU-scope 64-bit store and paired 64-bit load. Each aligned
 // 64-bit word is single-copy atomic: a reader sees it whole, old or new.
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
