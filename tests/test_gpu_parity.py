@@ -252,6 +252,23 @@ def test_ffn_given_routing_with_duplicates_and_bad_index(api, tiny):
     assert pu.rel_l2(pu.bf16_bits_to_f32(y), y_o) <= 1e-2
 
 
+@pytest.mark.parametrize("seed", [5, 91])
+def test_ffn_matches_layer_one_token(api, ling, seed):
+    """One token: the layer builds its plan one top-k round at a time (slots
+    in selection order) but sums the pairs in ascending expert order, so y is
+    bit-identical to moe_ffn run on the same routing (slots ascending)."""
+    s = api.make_shape(2560, 512, 8, 768, 768, 0)
+    x = synth.x_independent(synth.LING, seed, 1, device="cuda")
+    idx, w, y_layer, st = pu.run_layer(synth.LING, ling, x, 0)
+    assert st == 0
+    assert len(set(idx[0].tolist())) == 8
+    ws = api.workspace(s, 1)
+    y = torch.zeros((1, 2560), dtype=torch.bfloat16, device="cuda")
+    api.ffn(x, torch.from_numpy(idx).cuda(), torch.from_numpy(w).cuda(), pu.expert_weights_of(ling, 0), s, y, ws)
+    assert api.read_status(ws) == 0
+    assert torch.equal(y, y_layer)
+
+
 def test_ffn_matches_layer(api, ling):
     s = api.make_shape(2560, 512, 8, 768, 768, 0)
     M = 6
