@@ -156,7 +156,11 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.hr = reinterpret_cast<uint16_t*>(base + wl.hr);
 
     const size_t other_plan = align_up(sizeof(moe::Plan), 128);
-    const size_t x_bytes = align_up((size_t)M * p.H * 2, 128);
+    // one-token MXFP4 layers keep two copies of the tokens: f16 for the
+    // routed experts, bf16 for the router and the shared expert
+    const bool two = s->wfmt == 1 && M == 1 && mode == moe::kModeLayer;
+    const size_t x_one = align_up((size_t)M * p.H * 2, 128);
+    const size_t x_bytes = x_one * (two ? 2 : 1);
     // down-projection results per (pair, output row): [M + M*k][rpc]
     const size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
     const size_t bar_bytes = 128;
@@ -172,6 +176,7 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.off_plan = (uint32_t)off;
     off += other_plan;
     p.off_x = (uint32_t)off;
+    p.off_xb = (uint32_t)(off + (two ? x_one : 0));
     off += x_bytes;
     p.off_yacc = (uint32_t)off;
     off += y_bytes;

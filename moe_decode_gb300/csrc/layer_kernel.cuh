@@ -792,13 +792,17 @@ __device__ __forceinline__ void dot4_fp8(const uint8_t* const (&crow)[4], const 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // ------------------------------------------------------------ consumer
-template <int WFMT>
+// TWO: one-token MXFP4 launches, which hold the tokens twice, in f16 times
+// 2^s_t (swizzled) for the routed experts and in plain bf16 for the router
+// and the shared expert (the bf16 mixed-precision fma).
+template <int WFMT, bool TWO>
 struct Consumer {
     static constexpr int NCW = consumer_warps(WFMT);
     const LayerParams& p;
     Plan* plan;
     Ring ring;
     const uint16_t* xs;  // tokens in shared memory [M][H]
+    const uint16_t* xb;  // TWO: the same tokens in plain bf16
     float* ypair;        // down results per (pair, output row) [M + M*k][rpc]
     int warp, lane;
     int qm;              // rows go round-robin over the warps, continuing
@@ -821,6 +825,9 @@ struct Consumer {
     __device__ __forceinline__ const uint8_t* stage_ptr() const {
         return reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(ring.stage()));
     }
+    __device__ __forceinline__ const uint4* xbrow(int tok) const {
+        return reinterpret_cast<const uint4*>(xb + (size_t)tok * p.H);
+    }
     __device__ __forceinline__ const uint4* xrow(int tok) const {
         return reinterpret_cast<const uint4*>(xs + (size_t)tok * p.H);
     }
@@ -832,10 +839,15 @@ struct Consumer {
             const uint4* row = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             for (int t = 0; t < p.M; ++t) {
                 float acc[1];
-                const uint4* xt = xrow(t);
-                dot_bf16<1, 32, WFMT == 1, kXM<WFMT>>(row, xt, xt, nvec, lane, acc);
+                if (TWO) {
+                    const uint4* xt = xbrow(t);
+                    dot_bf16<1>(row, xt, xt, nvec, lane, acc);
+                } else {
+                    const uint4* xt = xrow(t);
+                    dot_bf16<1, 32, WFMT == 1, kXM<WFMT>>(row, xt, xt, nvec, lane, acc);
+                }
                 acc[0] = warp_sum(acc[0]);
-                if (WFMT == 1) acc[0] *= plan->x_inv[t];
+                if (WFMT == 1 && !TWO) acc[0] *= plan->x_inv[t];
                 // the logit and this call's tag in one 64-bit word: readers
                 // need no barrier, they wait for the tag
                 if (lane == 0)
@@ -851,7 +863,10 @@ struct Consumer {
         if (WFMT == 0 || shared) {
             const uint4* r1 = reinterpret_cast<const uint4*>(st + (size_t)j * p.H * 2);
             const uint4* r3 = reinterpret_cast<const uint4*>(st + (size_t)(ch.n + j) * p.H * 2);
-            dot2_bf16<NT, WFMT == 1, kXM<WFMT>>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
+            if (TWO)
+                dot2_bf16<NT>(r1, r3, xbrow(t0tok), xbrow(t1tok), p.H / 8, lane, g, u);
+            else
+                dot2_bf16<NT, WFMT == 1, kXM<WFMT>>(r1, r3, xrow(t0tok), xrow(t1tok), p.H / 8, lane, g, u);
         } else {
             const size_t cb = (size_t)p.H / (WFMT == 1 ? 2 : 1), sbytes = (size_t)p.H / 32;
             const uint4* c1 = reinterpret_cast<const uint4*>(st + j * cb);
@@ -892,7 +907,8 @@ struct Consumer {
                 float gs = warp_sum4(g[0], u[0], g[1], u[1], lane);
                 float us = __shfl_down_sync(0xffffffffu, gs, 8);
                 if ((lane & 15) == 0) {
-                    if (WFMT == 1) {  // tokens are held times 2^s_t
+                    // f16 tokens are held times 2^s_t (MXFP4)
+                    if (TWO ? !shared : WFMT == 1) {
                         const float xi = plan->x_inv[lane ? tb : ta];
                         gs *= xi, us *= xi;
                     }
@@ -906,7 +922,7 @@ struct Consumer {
                 float gs = warp_sum2(g[0], u[0], lane);
                 float us = __shfl_down_sync(0xffffffffu, gs, 16);
                 if (lane == 0) {
-                    if (WFMT == 1) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
+                    if (TWO ? !shared : WFMT == 1) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
                     hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(gs, us));
                 }
             }
@@ -1267,10 +1283,10 @@ static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, int
 // the token's largest magnitude (exact for bf16 values in f16's normal
 // range). Not inlined: it runs once per launch and keeps the kernel's other
 // code compact; its arguments are plain values.
-template <int WFMT>
+template <int WFMT, bool TWO>
 __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const uint4* __restrict__ gam, int M, int H,
-                                         float eps, uint4* __restrict__ dst, float* __restrict__ x_inv, int warp,
-                                         int lane, int nwarps) {
+                                         float eps, uint4* __restrict__ dst, uint4* __restrict__ dstb,
+                                         float* __restrict__ x_inv, int warp, int lane, int nwarps) {
     const int nvt = H / 8;
     for (int t = warp; t < M; t += nwarps) {
         const uint4* ht = src + (size_t)t * nvt;
@@ -1328,6 +1344,14 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
             v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
             v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
             dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
+            if (TWO) {  // the plain bf16 copy (the values are bf16 already)
+                uint4 b;
+                b.x = f32_to_bf16_bits(f[0]) | ((uint32_t)f32_to_bf16_bits(f[1]) << 16);
+                b.y = f32_to_bf16_bits(f[2]) | ((uint32_t)f32_to_bf16_bits(f[3]) << 16);
+                b.z = f32_to_bf16_bits(f[4]) | ((uint32_t)f32_to_bf16_bits(f[5]) << 16);
+                b.w = f32_to_bf16_bits(f[6]) | ((uint32_t)f32_to_bf16_bits(f[7]) << 16);
+                dstb[(size_t)t * nvt + i] = b;
+            }
         }
         if (lane == 0) x_inv[t] = exp2i(-sh);
     }
@@ -1462,7 +1486,9 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         // ---------------- consumers
         const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
-        Consumer<WFMT> cs{p, plan, ring0, xs, ypair, warp, lane, 0, h0};
+        constexpr bool TWO = ONE && WFMT == 1;
+        Consumer<WFMT, TWO> cs{p, plan, ring0, xs, reinterpret_cast<const uint16_t*>(smem + p.off_xb), ypair,
+                               warp, lane, 0, h0};
         pdl_wait();
         if (tid == 0) plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
         {
@@ -1470,8 +1496,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
             if (IO) {
-                load_tokens<WFMT>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.eps, dst,
-                                  plan->x_inv, warp, lane, NCW);
+                load_tokens<WFMT, TWO>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.eps, dst,
+                                       reinterpret_cast<uint4*>(smem + p.off_xb), plan->x_inv, warp, lane, NCW);
             } else if (WFMT == 0) {
                 for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
             } else if (WFMT == 2) {
@@ -1483,7 +1509,12 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             } else {
                 // MXFP4 layers hold the tokens in f16 times 2^s_t, s_t chosen
                 // from the token's largest magnitude (exact for bf16 values
-                // in f16's normal range)
+                // in f16's normal range); one-token launches also keep the
+                // plain bf16 copy
+                if (TWO) {
+                    uint4* dstb = reinterpret_cast<uint4*>(smem + p.off_xb);
+                    for (int i = tid; i < nv; i += NCT) dstb[i] = __ldg(src + i);
+                }
                 const int nvt = p.H / 8;
                 for (int t = warp; t < p.M; t += NCW) {
                     float mx = 0.f;

@@ -67,7 +67,10 @@ struct LayerParams {
     int force_timeout;
     unsigned long long timeout_ns;
     unsigned long long* trace;  // optional [G][16] phase timestamps (ns), may be null
-    uint32_t off_bar, off_plan, off_x, off_yacc, smem_bytes;
+    // shared-memory offsets: barriers, plan, tokens, a second copy of the
+    // tokens in plain bf16 (one-token MXFP4 launches; otherwise the same
+    // buffer), per-pair down results
+    uint32_t off_bar, off_plan, off_x, off_xb, off_yacc, smem_bytes;
 };
 
 // A unit of the ring: the tiles one stage holds. kind 0 router rows, 1
