@@ -61,9 +61,11 @@ __device__ __forceinline__ int swz_vec(int v, int xm) { return v ^ ((v >> 3) & x
 
 // ------------------------------------------------------------ chunk lists
 // The producer steps ChunkGen and writes each chunk's descriptor next to its
-// stage; the consumers read the descriptors and run no generator. Phases: 0 router rows, 1 shared-expert gate/up
-// rows, 2 routed gate/up rows (needs the plan), 3 down rows (needs the plan).
-// next() returns false at the end of each phase; begin(ph) starts a phase.
+// stage; the consumers read the descriptors and run no generator. Phases: 0
+// router rows, 1 shared-expert gate/up rows, 3 down rows (needs the plan);
+// the routed gate/up rows (phase 2) are claimed dynamically instead
+// (issue_routed_gateup). next() returns false at the end of each phase;
+// begin(ph) starts a phase.
 template <int WFMT>
 __device__ __forceinline__ int gateup_cap(const LayerParams& p, bool routed) {
     // a routed row pair: codes plus scales (MXFP4 and FP8 both carry H / 32
@@ -83,7 +85,6 @@ template <int WFMT>
 struct ChunkGen {
     int phase;
     int a, b, cap;                 // phases 0, 1: row cursor, end, rows per chunk
-    uint32_t r, r1, slot, i0, I;   // phase 2: flattened routed rows
     int ds, nslot, q0, npairs, pg, np, rcap, h, h0, h1;  // phase 3
 
     __device__ __forceinline__ void begin(int ph, const LayerParams& p, const Plan* plan, int c) {
@@ -97,14 +98,6 @@ struct ChunkGen {
             a = (int)(cc * (uint32_t)p.Is / G);
             b = (int)((cc + 1) * (uint32_t)p.Is / G);
             cap = gateup_cap<WFMT>(p, false);
-        } else if (ph == 2) {
-            I = (uint32_t)p.I;
-            const uint32_t R = (uint32_t)plan->nslot * I;  // <= 256 * 4096
-            r = (uint32_t)(((uint64_t)cc * R) / G);
-            r1 = (uint32_t)(((uint64_t)(cc + 1) * R) / G);
-            slot = r / I;
-            i0 = r - slot * I;
-            cap = gateup_cap<WFMT>(p, true);
         } else {
             nslot = plan->nslot;
             h0 = (int)(cc * (uint32_t)p.H / G);
@@ -125,18 +118,6 @@ struct ChunkGen {
             const int n = min(cap, b - a);
             ch = Chunk{phase == 0 ? 0 : 1, -1, a, n, 0, 0};
             a += n;
-            return true;
-        }
-        if (phase == 2) {
-            if (r >= r1) return false;
-            const uint32_t n = min((uint32_t)cap, min(r1 - r, I - i0));
-            ch = Chunk{1, (int)slot, (int)i0, (int)n, 0, 0};
-            r += n;
-            i0 += n;
-            if (i0 == I) {
-                i0 = 0;
-                ++slot;
-            }
             return true;
         }
         // phase 3: slots (shared first), pair groups, row chunks

@@ -48,18 +48,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// As mbar_try_wait, with a bound (ns) on how long the thread may stay
-// suspended before the probe returns false.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Non-blocking probe of the same condition.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -233,21 +221,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t v, uint32_t& lo, uint32
         : "r"(v));
 }
 
-// Sixteen e4m3 codes (one uint4) as fp32.
-__device__ __forceinline__ void unpack16_e4m3(const uint4 c, float (&f)[16]) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint32_t lo, hi;
-        e4m3x4_to_f16x2(w[k], lo, hi);
-        const float2 a = f16x2_to_f32(lo), b = f16x2_to_f32(hi);
-        f[4 * k + 0] = a.x;
-        f[4 * k + 1] = a.y;
-        f[4 * k + 2] = b.x;
-        f[4 * k + 3] = b.y;
-    }
-}
-
 // Sixteen e4m3 codes (one uint4) as eight f16 pairs: w[j] holds codes 2j
 // (low half) and 2j + 1. Every e4m3 value is exact in f16.
 __device__ __forceinline__ void e4m3x16_to_f16x2(const uint4 c, uint32_t (&w)[8]) {
@@ -257,7 +230,7 @@ __device__ __forceinline__ void e4m3x16_to_f16x2(const uint4 c, uint32_t (&w)[8]
     e4m3x4_to_f16x2(c.w, w[6], w[7]);
 }
 
-// The same sixteen values as eight (even, odd) pairs.
+// Sixteen e4m3 codes (one uint4) as eight fp32 (even, odd) pairs.
 __device__ __forceinline__ void unpack16_e4m3x2(const uint4 c, float2 (&f)[8]) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
