@@ -95,6 +95,34 @@ def test_lm_head_small_ragged(api, M, wfmt):
     assert rel_l2(got, want) <= TOL
 
 
+@pytest.mark.parametrize("wfmt", [0, 2])
+def test_lm_head_token_scales(api, wfmt):
+    """Tokens of very different magnitudes (and an all-zero one) in one call:
+    FP8 launches hold each token in f16 times its own power of two, which must
+    come back out of that token's logits, also within a token pair."""
+    V, H, M = 700, 512, 5
+    Wb = synth.normal_bf16(61, 1, 0, V * H, 0.02, "cuda").view(V, H)
+    x = synth.normal_bf16(62, 2, 0, M * H, 1.0, "cuda").view(M, H).float()
+    x[0] *= 1e-3
+    x[1] *= 1e3
+    x[2] = 0.0
+    x[4] *= 37.0
+    x = x.to(torch.bfloat16)
+    if wfmt == 0:
+        got = _run_lm(api, x, Wb, V, H, 0)
+        want = oracle.lm_head(synth.to_u16(x), synth.to_u16(Wb), V)
+    else:
+        codes = torch.empty((V, H), dtype=torch.uint8, device="cuda")
+        scales = torch.empty((V, 1), dtype=torch.float32, device="cuda")
+        api.fp8_quantize(Wb, H, codes, scales)
+        got = _run_lm(api, x, codes, V, H, 2, scales.view(V))
+        c_o, s_o = oracle.fp8_quantize(synth.to_u16(Wb), H)
+        want = oracle.lm_head(synth.to_u16(x), c_o, V, wfmt=2, scale=s_o[:, 0])
+    assert np.all(got[2] == 0.0)
+    for t in (0, 1, 3, 4):  # each token against its own reference
+        assert rel_l2(got[t], want[t]) <= TOL, t
+
+
 def test_lm_head_fewer_rows_than_ctas(api):
     V, H, M = 7, 512, 5
     Wb = synth.normal_bf16(41, 1, 0, V * H, 0.02, "cuda").view(V, H)
