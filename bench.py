@@ -7,9 +7,12 @@ the 129 MB L2, so every step streams its experts from HBM. Inputs are seeded
 synthetic data (moe_decode_gb300.synth); nothing is read from disk.
 
 Headline line: Ling-shape layer (H=2560, E=512, top-8, I=768, one shared
-expert), bf16 weights, M=1, 4 rotated layer copies. The other workloads
-(M=6 independent tokens, M=10 with ~50% consecutive overlap, MXFP4 experts at
-M=1 and M=6) are measured in the same run and reported under "also".
+expert), bf16 weights, M=1. The number of rotated layer copies is derived
+from the device's L2 size: a copy is reused only after more than 3 x L2 bytes
+of other copies' weights were streamed (checked after the routing pass). The
+other workloads (M=6 independent tokens, M=10 with ~50% consecutive overlap,
+the M=1..16 verify-length sweep, MXFP4 and FP8 experts at M=1 and M=6, the
+output layer) are measured in the same run and reported under "also".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -34,19 +37,28 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE decode layer µs/step and achieved HBM GB/s (cold weights) at M=1/6/10"
 PERIOD = 64  # input ring length; the copy rotation divides it
 
+# copies: layer copies rotated per step. The full-size workloads use at least
+# as many as the cold-weight rule needs (see cold_copies); the small profiling
+# cases keep a fixed, small count.
 WORKLOADS = {
     "ling_m1": dict(M=1, wfmt=0, copies=4, gen="independent"),
     "ling_m6": dict(M=6, wfmt=0, copies=4, gen="independent"),
     "ling_m10": dict(M=10, wfmt=0, copies=4, gen="overlap"),
     "mxfp4_m1": dict(M=1, wfmt=1, copies=8, gen="independent"),
     "mxfp4_m6": dict(M=6, wfmt=1, copies=8, gen="independent"),
-    "fp8_m1": dict(M=1, wfmt=2, copies=6, gen="independent"),
-    "fp8_m6": dict(M=6, wfmt=2, copies=6, gen="independent"),
-    # small case for detailed profiler captures: the Ling layer cut to 128
+    "fp8_m1": dict(M=1, wfmt=2, copies=8, gen="independent"),
+    "fp8_m6": dict(M=6, wfmt=2, copies=8, gen="independent"),
+    # small cases for detailed profiler captures: the Ling layer cut to 128
     # experts (1.5 GB per copy), still far above L2
-    "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128),
-    "mxfp4_e128_m6": dict(M=6, wfmt=1, copies=2, gen="independent", E=128),
+    "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128, fixed_copies=True),
+    "ling_e128_m10": dict(M=10, wfmt=0, copies=2, gen="overlap", E=128, fixed_copies=True),
+    "mxfp4_e128_m6": dict(M=6, wfmt=1, copies=2, gen="independent", E=128, fixed_copies=True),
+    "fp8_e128_m6": dict(M=6, wfmt=2, copies=2, gen="independent", E=128, fixed_copies=True),
 }
+# the verify-length sweep: M = 1..16 tokens with ~50% consecutive top-8 overlap
+for _m in range(1, 17):
+    WORKLOADS[f"sweep_m{_m}"] = dict(M=_m, wfmt=0, copies=4, gen="overlap")
+SWEEP = ",".join(f"sweep_m{m}" for m in range(1, 17))
 
 
 # output layer (lm_head): the model's 157,184 x 2,560 vocabulary matrix (805 MB
@@ -64,7 +76,37 @@ def layer_shape(name: str):
     return synth.LayerShape(synth.LING.hidden, E, synth.LING.top_k, synth.LING.inter, synth.LING.shared_inter)
 
 
-def describe(name: str) -> str:
+def expert_bytes(shape, wfmt: int) -> int:
+    H, I = shape.hidden, shape.inter
+    if wfmt == 0:
+        return 3 * H * I * 2
+    if wfmt == 1:
+        return 2 * (I * H // 2 + I * H // 32) + (H * I // 2 + H * I // 32)
+    return 3 * (H * I + H * I // 128 * 4)
+
+
+def min_step_bytes(shape, wfmt: int, M: int) -> int:
+    """Fewest algorithmic bytes a step can touch: the router, the shared
+    expert and the k experts of one token (|U| >= k)."""
+    return (shape.n_experts * shape.hidden * 2 + shape.top_k * expert_bytes(shape, wfmt)
+            + 3 * shape.hidden * shape.shared_inter * 2 + 4 * M * shape.hidden)
+
+
+def cold_copies(name: str, l2_bytes: int) -> int:
+    """Layer copies rotated per step so that weights are cold: a copy is
+    reused only after more than 3 x L2 bytes of other copies' weights were
+    streamed. The count is a power of two (it divides the input ring)."""
+    w = WORKLOADS[name]
+    c = w["copies"]
+    if w.get("fixed_copies"):
+        return c
+    need = 3 * l2_bytes / min_step_bytes(layer_shape(name), w["wfmt"], w["M"])
+    while c - 1 <= need:
+        c *= 2
+    return c
+
+
+def describe(name: str, copies: int) -> str:
     w = WORKLOADS[name]
     E = w.get("E", 512)
     fmt = {0: "bf16", 1: "MXFP4 (e2m1 + e8m0/32) routed experts, bf16 router and shared expert",
@@ -72,7 +114,7 @@ def describe(name: str) -> str:
     gen = ("tokens drawn independently" if w["gen"] == "independent"
            else "tokens with ~50% consecutive top-8 overlap")
     return (f"Ling-shape MoE layer H=2560 E={E} top-8 I=768 shared I=768, {fmt}, M={w['M']} ({gen}), "
-            f"cold weights rotated over {w['copies']} layer copies")
+            f"cold weights rotated over {copies} layer copies")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -135,7 +177,10 @@ class ClockSampler:
             self.t.start()
         except Exception:
             self.proc = None
-        time.sleep(0.25)
+        # wait (at most 3 s) until the sampler is running
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < 3.0:
+            time.sleep(0.01)
         return self
 
     def _read(self):
@@ -185,17 +230,40 @@ def visible_gpu_index(local_rank: int) -> int:
 
 # ----------------------------------------------------------------------------- our arm
 
+class LayerCache:
+    """Device layer copies shared by the workloads of one run that use the
+    same shape and weight format (the M sweep reuses one set)."""
+
+    def __init__(self):
+        self.sets = {}
+
+    def get(self, sh, wfmt: int, copies: int, device):
+        key = (sh, wfmt)
+        have = self.sets.get(key, [])
+        from moe_decode_gb300 import synth
+        while len(have) < copies:
+            have.append(synth.device_layer(sh, len(have), wfmt, device))
+        self.sets[key] = have
+        return have[:copies]
+
+    def drop_except(self, keep_key=None):
+        for k in list(self.sets):
+            if k != keep_key:
+                del self.sets[k]
+
+
 class Workload:
-    def __init__(self, name: str, device):
+    def __init__(self, name: str, device, cache: LayerCache, l2_bytes: int):
         from moe_decode_gb300 import api, synth
         self.api, self.synth = api, synth
         self.name = name
         w = WORKLOADS[name]
-        self.M, self.wfmt, self.ncopy = w["M"], w["wfmt"], w["copies"]
+        self.M, self.wfmt = w["M"], w["wfmt"]
+        self.ncopy = cold_copies(name, l2_bytes)
         sh = layer_shape(name)
         self.shape = sh
         self.cshape = api.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.inter, sh.shared_inter, self.wfmt)
-        self.layers = [synth.device_layer(sh, c, self.wfmt, device) for c in range(self.ncopy)]
+        self.layers = cache.get(sh, self.wfmt, self.ncopy, device)
         self.weights = [api.ExpertWeights(w1=L["w1"], w3=L["w3"], w2=L["w2"], ws1=L["ws1"], ws3=L["ws3"],
                                           ws2=L["ws2"], s1=L.get("s1"), s3=L.get("s3"), s2=L.get("s2"))
                         for L in self.layers]
@@ -231,56 +299,73 @@ class Workload:
         """Algorithmic HBM bytes of step s: router + touched experts + shared
         expert + x in + y out + routing out."""
         sh = self.shape
-        H, I, E = sh.hidden, sh.inter, sh.n_experts
+        H, E = sh.hidden, sh.n_experts
         U = int(self.distinct[s % PERIOD])
-        if self.wfmt == 0:
-            expert = 3 * H * I * 2
-        elif self.wfmt == 1:
-            expert = 2 * (I * H // 2 + I * H // 32) + (H * I // 2 + H * I // 32)
-        else:
-            expert = 3 * (H * I + H * I // 128 * 4)
         shared = 3 * H * sh.shared_inter * 2
-        return E * H * 2 + U * expert + shared + 2 * self.M * H * 2 + self.M * sh.top_k * 8
+        return E * H * 2 + U * expert_bytes(sh, self.wfmt) + shared + 2 * self.M * H * 2 + self.M * sh.top_k * 8
 
     def mean_bytes(self, K: int) -> float:
         return sum(self.step_bytes(s) for s in range(K)) / K
 
+    def reuse_bytes_min(self) -> float:
+        """Fewest weight bytes streamed between two uses of one copy: the
+        other copies' steps in between (ncopy - 1 of them)."""
+        per = sorted(self.step_bytes(s) for s in range(PERIOD))
+        return float(sum(per[:self.ncopy - 1]))
+
 
 class LmWorkload:
-    """Output-layer GEMV: logits [M, V] of M tokens (one launch per step)."""
+    """Output-layer GEMV: logits [M, V] of M tokens (one launch per step).
+    Every step reads the whole matrix, so between two reads of a weight byte
+    at least one full pass over its own copy is streamed; copies are added
+    (rotated per step) until that exceeds 3 x L2."""
 
-    def __init__(self, name: str, device):
+    def __init__(self, name: str, device, cache=None, l2_bytes: int = 0):
         from moe_decode_gb300 import api, synth
         self.api = api
         self.name = name
         w = LM_WORKLOADS[name]
         self.M, self.wfmt, self.V, self.H = w["M"], w["wfmt"], w["V"], w["H"]
-        Wb = synth.normal_bf16(3000, 1, 0, self.V * self.H, synth.WEIGHT_SIGMA, device).view(self.V, self.H)
-        if self.wfmt == 0:
-            self.W, self.scale = Wb, None
-        else:
-            self.W = torch.empty((self.V, self.H), dtype=torch.uint8, device=device)
-            self.scale = torch.empty((self.V, 1), dtype=torch.float32, device=device)
-            api.fp8_quantize(Wb, self.H, self.W, self.scale)
-            del Wb
+        per_copy = self.V * self.H * (2 if self.wfmt == 0 else 1)
+        self.ncopy = 1
+        while self.ncopy * per_copy <= 3 * l2_bytes:
+            self.ncopy *= 2
+        self.W, self.scale = [], []
+        for c in range(self.ncopy):
+            Wb = synth.normal_bf16(3000 + c, 1, 0, self.V * self.H, synth.WEIGHT_SIGMA, device).view(self.V, self.H)
+            if self.wfmt == 0:
+                self.W.append(Wb)
+                self.scale.append(None)
+            else:
+                q = torch.empty((self.V, self.H), dtype=torch.uint8, device=device)
+                sc = torch.empty((self.V, 1), dtype=torch.float32, device=device)
+                api.fp8_quantize(Wb, self.H, q, sc)
+                del Wb
+                self.W.append(q)
+                self.scale.append(sc.view(-1))
         self.xs = torch.stack([synth.x_independent(synth.LING, s, self.M, device=device) for s in range(PERIOD)])
         self.logits = torch.empty((self.M, self.V), dtype=torch.float32, device=device)
         self.ws = torch.empty(api.LM_HEAD_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
         api.workspace_init(self.ws)
-        self.weight_bytes = self.W.numel() * self.W.element_size()
+        self.copy_bytes = per_copy
+        self.weight_bytes = per_copy * self.ncopy
         self.distinct = np.zeros(1)
 
     def step(self, s: int, stream, idx=None, w=None, x=None, y=None):
-        self.api.lm_head(self.xs[s % PERIOD] if x is None else x, self.W, self.V, self.H, self.logits, self.ws,
-                         wfmt=self.wfmt, w_scale=None if self.scale is None else self.scale.view(-1), stream=stream)
+        c = s % self.ncopy
+        self.api.lm_head(self.xs[s % PERIOD] if x is None else x, self.W[c], self.V, self.H, self.logits, self.ws,
+                         wfmt=self.wfmt, w_scale=self.scale[c], stream=stream)
 
     def routing_pass(self, stream):
         self.step(0, stream)
         stream.synchronize()
 
+    def reuse_bytes_min(self) -> float:
+        return float(self.ncopy * self.copy_bytes)
+
     def mean_bytes(self, K: int) -> float:
         """Weights (+ e4m3 row scales), tokens in, logits out."""
-        return self.weight_bytes + (self.V * 4 if self.wfmt else 0) + self.M * self.H * 2 + self.M * self.V * 4
+        return self.copy_bytes + (self.V * 4 if self.wfmt else 0) + self.M * self.H * 2 + self.M * self.V * 4
 
 
 def capture_graph(wl: Workload, start: int, n: int, stream):
@@ -311,17 +396,22 @@ def time_device(wl: Workload, K: int, W: int, stream, use_graph: bool, dist_barr
             torch.cuda.synchronize()
             print(f"# graph capture failed ({e}); timing stream launches", file=sys.stderr)
             graphs = None
-    for s in range(W):
-        wl.step(s, stream)
-    if graphs:
-        graphs[0].replay()
-    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    dist_barrier()
-    torch.cuda.synchronize()
     ctx = sampler if sampler is not None else _Null()
     with ctx:
+        # the W warm-up steps (and one replay of the timed graph) run right
+        # before the timed region, inside the clock sampler's context: an
+        # idle GPU (e.g. while the sampler starts) would make the first
+        # timed steps slower, which a short timed region cannot amortise
+        for s in range(W):
+            wl.step(s, stream)
+        if graphs:
+            with torch.cuda.stream(stream):
+                graphs[0].replay()
+        torch.cuda.synchronize()
+        dist_barrier()
+        torch.cuda.synchronize()
         # NVTX range "timed_region": lets a profiler's launch list cover
         # exactly the timed steps (ncu --nvtx --nvtx-include timed_region/)
         torch.cuda.nvtx.range_push("timed_region")
@@ -434,11 +524,12 @@ def cpu_steps_for(name: str) -> int:
     return max(1, int(12.0 / per_step_s))
 
 
-def oracle_sample(wl: Workload, nsteps: int):
-    """Times the CPU oracle (as it stands, one host thread) on `nsteps` steps
-    of the workload. Each step's host copies of its touched experts are made
-    before that step's clock starts; only the oracle calls are timed.
-    Returns us per step."""
+def oracle_sample(wl: Workload, nsteps: int, nthreads: int = 1):
+    """Times the CPU oracle (as it stands) on `nsteps` steps of the workload:
+    in one host thread (nthreads 1), or with its expert calls spread over
+    host threads (0: all; the same arithmetic and bits). Each step's host
+    copies of its touched experts are made before that step's clock starts;
+    only the oracle calls are timed. Returns us per step."""
     import oracle
     oracle.build()
     sh, synth = wl.shape, wl.synth
@@ -456,7 +547,7 @@ def oracle_sample(wl: Workload, nsteps: int):
         missing = [int(e) for e in np.unique(idx) if int(e) not in experts]
         if missing:
             raise RuntimeError(f"oracle routed to experts {missing} the device did not")
-        oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, shared[c], wfmt=wl.wfmt)
+        oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, shared[c], wfmt=wl.wfmt, nthreads=nthreads)
         dt += time.perf_counter() - t0
     return dt / nsteps * 1e6
 
@@ -485,7 +576,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="ling_m1")
     ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,fp8_m1,fp8_m6,"
-                                      "lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6",
+                                      "lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6," + SWEEP,
                     help="comma-separated extra workloads measured in the same run ('' for none)")
     ap.add_argument("--cpu-steps", type=int, default=0,
                     help="oracle steps timed for cpu_baseline (0: about 12 s of oracle work for the workload)")
@@ -517,12 +608,25 @@ def main():
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
     stream = torch.cuda.Stream(device)
+    l2_bytes = int(torch.cuda.get_device_properties(device).L2_cache_size)
 
     results = {}
     names = [args.workload] + [n for n in args.also.split(",") if n and n != args.workload]
+    cache = LayerCache()
     for name in names:
-        wl = LmWorkload(name, device) if name in LM_WORKLOADS else Workload(name, device)
+        if name in LM_WORKLOADS:
+            cache.drop_except()
+            wl = LmWorkload(name, device, l2_bytes=l2_bytes)
+        else:
+            cache.drop_except((layer_shape(name), WORKLOADS[name]["wfmt"]))
+            wl = Workload(name, device, cache, l2_bytes)
         wl.routing_pass(stream)
+        # cold weights: a copy is reused only after > 3 x L2 bytes of others
+        reuse = wl.reuse_bytes_min()
+        if not WORKLOADS.get(name, {}).get("fixed_copies") and reuse <= 3 * l2_bytes:
+            # (the profiling cases keep a small, fixed rotation on purpose)
+            raise RuntimeError(f"{name}: only {reuse / 1e6:.0f} MB between reuses of a layer copy "
+                               f"(<= 3 x L2 = {3 * l2_bytes / 1e6:.0f} MB)")
         main_run = name == args.workload
         sampler = ClockSampler(visible_gpu_index(local_rank)) if main_run else None
         K = args.steps if main_run else min(args.steps, 4096)
@@ -535,7 +639,7 @@ def main():
         res = {"us_per_step": us_job, "us_per_step_per_replica": us_step,
                "hbm_gbs": nbytes / (us_step * 1e-6) / 1e9, "bytes_per_step": nbytes,
                "distinct_experts_mean": float(np.mean(wl.distinct)), "steps": K, "launch": mode,
-               "weights_gb": wl.weight_bytes / 1e9}
+               "weights_gb": wl.weight_bytes / 1e9, "copies": wl.ncopy, "reuse_bytes_min": reuse}
         if main_run:
             res["clocks"] = sampler.summary()
             e2e_ms, h2d, d2h = time_e2e(wl, K, stream, zero_copy=True)
@@ -546,11 +650,15 @@ def main():
                                   "and writes y over the coherent CPU-GPU link (steps replayed as CUDA graphs)",
                           "explicit_copies_us_per_step": e2c_ms * 1e3 / K}
             if rank == 0:
+                import oracle
                 res["cpu_steps"] = args.cpu_steps or cpu_steps_for(name)
                 res["cpu_us"] = oracle_sample(wl, res["cpu_steps"])
+                res["cpu_all_us"] = oracle_sample(wl, res["cpu_steps"], nthreads=0)
+                res["cpu_threads"] = oracle.threads()
         results[name] = res
         del wl
         torch.cuda.empty_cache()
+    cache.drop_except()
 
     if rank != 0:
         return
@@ -559,6 +667,7 @@ def main():
     achieved = main_res["hbm_gbs"]
     w = WORKLOADS[args.workload]
     traffic = traffic_record("moe_layer_kernel", args.workload)
+    tasks = w["M"] * (layer_shape(args.workload).top_k + 1)
     line = {
         "metric": METRIC,
         "value": round(main_res["us_per_step"], 3),
@@ -572,13 +681,7 @@ def main():
         "vs_baseline": None,
         "dtype": {0: "bf16", 1: "mxfp4-weights/bf16-act", 2: "fp8-e4m3-weights/bf16-act"}[w["wfmt"]],
         "data": "synthetic (seeded counter-hash generator; N(0,0.02)-like weights, N(0,1)-like tokens)",
-        "config": {"workload": describe(args.workload), "M": w["M"], "hidden": 2560,
-                   "n_experts": w.get("E", 512),
-                   "top_k": 8, "inter": 768, "shared_inter": 768, "layer_copies": w["copies"],
-                   "weights_gb": round(main_res["weights_gb"], 2),
-                   "l2": "inputs larger than L2 (layer copies rotated every step)",
-                   "launch": main_res["launch"], "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "distinct_experts_mean": main_res["distinct_experts_mean"]},
+        "config": workload_config(args.workload, main_res["copies"], world, main_res, l2_bytes),
         "hbm_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
@@ -586,16 +689,39 @@ def main():
         "cpu_baseline": {"value": round(main_res["cpu_us"], 1), "unit": "us/step", "cores": 1,
                          "kind": "oracle",
                          "sample": f"{main_res['cpu_steps']} steps of the same workload (same inputs, routing "
-                                   f"and touched experts), oracle in one host thread"},
+                                   f"and touched experts), oracle in one host thread",
+                         "all_cores": {"value": round(main_res["cpu_all_us"], 1), "unit": "us/step",
+                                       "cores": min(main_res["cpu_threads"], tasks),
+                                       "host_cpus": os.cpu_count(), "threads_available": main_res["cpu_threads"],
+                                       "sample": f"the same {main_res['cpu_steps']} steps; the oracle's "
+                                                 f"{tasks} (token, expert) calls per step (the shared expert "
+                                                 f"included) spread over OpenMP threads, same bits"}},
         "e2e": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in main_res["e2e"].items()},
         "gpu_launches": args.steps,
         "clocks": main_res["clocks"],
         "also": {n: {k: (round(v, 3) if isinstance(v, float) else v) for k, v in r.items()
-                     if k in ("us_per_step", "hbm_gbs", "distinct_experts_mean", "steps", "launch")}
+                     if k in ("us_per_step", "hbm_gbs", "distinct_experts_mean", "steps", "launch", "copies")}
                  | {"roofline_frac": round(r["hbm_gbs"] / peak, 4)}
                  for n, r in results.items() if n != args.workload},
     }
     print(json.dumps(line))
+
+
+def workload_config(name: str, copies: int, world: int, res=None, l2_bytes: int = 0) -> dict:
+    """The bench line's config for a layer workload (the same dict on the
+    reference arm)."""
+    w = WORKLOADS[name]
+    cfg = {"workload": describe(name, copies), "M": w["M"], "hidden": 2560, "n_experts": w.get("E", 512),
+           "top_k": 8, "inter": 768, "shared_inter": 768, "layer_copies": copies,
+           "l2": "inputs larger than L2 (layer copies rotated every step)",
+           "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+    if res is not None:
+        cfg["weights_gb"] = round(res["weights_gb"], 2)
+        cfg["launch"] = res["launch"]
+        cfg["distinct_experts_mean"] = res["distinct_experts_mean"]
+        cfg["cold_weights"] = {"l2_bytes": l2_bytes, "bytes_between_reuses_min": int(res["reuse_bytes_min"]),
+                               "rule": "bytes streamed between two uses of a layer copy > 3 x L2"}
+    return cfg
 
 
 def run_reference(args, rank: int, world: int):
@@ -613,10 +739,13 @@ def run_reference(args, rank: int, world: int):
     gen = synth.x_independent if w["gen"] == "independent" else synth.x_overlap
     copies = {}
     wsteps = min(args.warmup, 3)
+    # the same layer-copy rotation as the GPU arm (it depends on the L2 size)
+    l2_bytes = int(torch.cuda.get_device_properties(0).L2_cache_size) if dev == "cuda" else 126 << 20
+    copies_ref = cold_copies(args.workload, l2_bytes)
 
     def prepare(s):
         """Inputs of step s and host copies of the experts it touches."""
-        c = s % w["copies"]
+        c = s % copies_ref
         if c not in copies:
             copies[c] = (synth.to_u16(synth.router_weight(sh, c, dev)),
                          tuple(synth.to_u16(m) for m in synth.shared_weights(sh, c, dev)))
@@ -652,7 +781,7 @@ def run_reference(args, rank: int, world: int):
     line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32-accumulate (oracle)", "data": "synthetic",
-            "config": {"workload": describe(args.workload), "M": w["M"]},
+            "config": workload_config(args.workload, copies_ref, world),
             "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

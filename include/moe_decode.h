@@ -88,12 +88,14 @@ extern "C" {
                                         that (token, slot) was skipped */
 #define MOE_ETIMEOUT (-101)          /* a bounded device wait ran out; the
                                         call's outputs are incomplete and the
-                                        workspace must be re-initialised */
+                                        workspace must be re-initialised:
+                                        until then every call on it refuses
+                                        to run and reports MOE_ETIMEOUT */
 
 /* flags of moe_decode_layer */
 #define MOE_F_NO_PDL 1u                /* launch without programmatic
                                           dependent launch */
-#define MOE_F_RESET_SCRATCH 2u          /* moe_decode_layer_static_scratch
+#define MOE_F_RESET_SCRATCH 2u         /* moe_decode_layer_static_scratch
                                           only: zero the static scratch
                                           before the launch */
 #define MOE_F_DEBUG_FORCE_TIMEOUT 256u /* test hook: the routing step waits
@@ -197,22 +199,32 @@ int moe_decode_layer(const void* x, int M, const void* Wg,
  * arithmetic as moe_decode_layer (so the same outputs, bit for bit), but the
  * workspace is a fixed array of MOE_STATIC_SCRATCH_BYTES in the library's
  * own device memory (one per device, created when the module loads). The
- * call allocates and frees nothing; its first call on a device looks the
- * array up and zeroes it on `stream`.
+ * call allocates and frees nothing. Every call looks the array's device
+ * address up again (cudaGetSymbolAddress, which allocates nothing); the
+ * first call on a device, and the first after a device reset moved the
+ * array, zeroes it on `stream`.
  *  - Returns MOE_ESCRATCH, before touching the device, when the shape and M
  *    need more than MOE_STATIC_SCRATCH_BYTES of workspace
  *    (moe_workspace_bytes > MOE_STATIC_SCRATCH_BYTES).
  *  - All calls on a device share the one scratch: they must be ordered on
  *    one stream (or otherwise serialised), also against other threads.
- *  - flags: MOE_F_NO_PDL, MOE_F_RESET_SCRATCH (needed again only after a
- *    bounded device wait ran out). The device status word of these calls
- *    lives in the scratch and is not readable through this ABI.
+ *  - flags: MOE_F_NO_PDL, MOE_F_DEBUG_FORCE_TIMEOUT, MOE_F_RESET_SCRATCH
+ *    (zeroes the scratch before the launch).
+ *  - Failure detection: the device status word lives in the scratch; read it
+ *    with moe_static_scratch_status. After MOE_ETIMEOUT every later call
+ *    refuses to run (it reports MOE_ETIMEOUT again and leaves its outputs
+ *    unwritten) until one is made with MOE_F_RESET_SCRATCH.
  * Other arguments, layouts and errors as moe_decode_layer. */
 int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg,
                                     const moe_weights* weights,
                                     const moe_shape* shape, int32_t* idx_out,
                                     float* w_out, void* y, uint32_t flags,
                                     void* stream);
+
+/* Synchronises `stream`, then copies the device status word of this
+ * device's static scratch (moe_decode_layer_static_scratch) to *dev_status:
+ * MOE_OK or a device code. Allocates nothing; not for the hot path. */
+int moe_static_scratch_status(void* stream, int32_t* dev_status);
 
 /* ------------------------------------------------------------ output layer
  * Output layer (lm_head) GEMV for M = 1..16 tokens: logits fp32 [M, V] =

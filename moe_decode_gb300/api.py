@@ -65,6 +65,7 @@ def _load():
     lib.moe_decode_layer.argtypes = [P, I32, P, wp, sp, P, P, P, P, SZ, ctypes.c_uint32, P]
     lib.moe_decode_layer_static_scratch.argtypes = [P, I32, P, wp, sp, P, P, P, ctypes.c_uint32, P]
     lib.moe_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.moe_static_scratch_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
     lib.moe_status_str.argtypes = [I32]
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_mxfp4_dequant.argtypes = [P, P, I64, I32, P, P]
@@ -74,7 +75,7 @@ def _load():
     lib.moe_fp8_dequant.argtypes = [P, P, I64, I32, I32, P, P]
     lib.moe_last_launch_count.argtypes = []
     for f in ("moe_workspace_init", "moe_route", "moe_ffn", "moe_decode_layer", "moe_decode_layer_static_scratch",
-              "moe_read_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count",
+              "moe_read_status", "moe_static_scratch_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count",
               "moe_lm_head", "moe_fp8_quantize", "moe_fp8_dequant"):
         getattr(lib, f).restype = I32
     return lib
@@ -181,6 +182,13 @@ def decode_layer_static_scratch(x, Wg, weights: ExpertWeights, shape: Shape, y, 
 def read_status(ws, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check(lib.moe_read_status(_ptr(ws), _stream(stream), ctypes.byref(v)), "moe_read_status")
+    return v.value
+
+
+def static_scratch_status(stream=None) -> int:
+    """Device status word of this device's static scratch (synchronises)."""
+    v = ctypes.c_int32(0)
+    _check(lib.moe_static_scratch_status(_stream(stream), ctypes.byref(v)), "moe_static_scratch_status")
     return v.value
 
 

@@ -60,25 +60,30 @@ int device_info(DeviceInfo* out) {
 
 void* g_scratch_ptr[kMaxDevices];
 
-// Device address of this device's static scratch; the first call on a device
-// looks it up and zeroes it on `st`.
+// Device address of this device's static scratch. cudaGetSymbolAddress is
+// called on every call (it allocates nothing): after a device reset the
+// module is loaded again and the array may sit elsewhere. The first call on a
+// device, and the first after the address changed, zeroes the array on `st`.
 int static_scratch(void** out, cudaStream_t st) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return MOE_ENODEVICE;
     }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
     std::lock_guard<std::mutex> lk(g_dev_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress((void**)&ptr, g_static_scratch) != cudaSuccess ||
-            cudaMemsetAsync(ptr, 0, MOE_STATIC_SCRATCH_BYTES, st) != cudaSuccess) {
+    if (g_scratch_ptr[dev] != ptr) {
+        if (cudaMemsetAsync(ptr, 0, MOE_STATIC_SCRATCH_BYTES, st) != cudaSuccess) {
             cudaGetLastError();
             return MOE_ECUDA;
         }
         g_scratch_ptr[dev] = ptr;
     }
-    *out = g_scratch_ptr[dev];
+    *out = ptr;
     return MOE_OK;
 }
 
@@ -164,7 +169,9 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     // down-projection results per (pair, output row): [M + M*k][rpc]
     const size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
     const size_t bar_bytes = 128;
-    size_t fixed = other_plan + x_bytes + y_bytes + bar_bytes;
+    // the router's selection bias, staged before the dependency wait
+    const size_t bias_bytes = s->router_bias ? align_up((size_t)s->n_experts * 4, 128) : 0;
+    size_t fixed = other_plan + x_bytes + y_bytes + bar_bytes + bias_bytes;
     if ((size_t)dev.smem_optin <= fixed) return MOE_ESHAPE;
     int ns = (int)(((size_t)dev.smem_optin - fixed) / moe::kStageBytes);
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;
@@ -180,6 +187,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     off += x_bytes;
     p.off_yacc = (uint32_t)off;
     off += y_bytes;
+    p.off_bias = (uint32_t)off;
+    off += bias_bytes;
     p.smem_bytes = (uint32_t)off;
     return MOE_OK;
 }
@@ -308,7 +317,7 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     g_last_launches = 0;
     int rc = check_shape(shape, M);
     if (rc) return rc;
-    if (flags & ~(MOE_F_NO_PDL | MOE_F_RESET_SCRATCH)) return MOE_EINVAL;
+    if (flags & ~(MOE_F_NO_PDL | MOE_F_RESET_SCRATCH | MOE_F_DEBUG_FORCE_TIMEOUT)) return MOE_EINVAL;
     if (ws_layout(shape, M).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ESCRATCH;
     if (!x || !Wg || !y || !weights_ok(weights, shape)) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(y) || !weights_aligned(weights, shape)) return MOE_EALIGN;
@@ -329,8 +338,17 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     p.idx_out = idx_out;
     p.w_out = w_out;
     p.y = static_cast<uint16_t*>(y);
+    p.force_timeout = (flags & MOE_F_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
     set_weights(p, weights);
     return launch(p, shape->wfmt, st, (flags & MOE_F_NO_PDL) == 0, dev);
+}
+
+int moe_static_scratch_status(void* stream, int32_t* dev_status) {
+    if (!dev_status) return MOE_EINVAL;
+    void* ws = nullptr;
+    const int rc = static_scratch(&ws, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
+    return moe_read_status(ws, stream, dev_status);
 }
 
 int moe_lm_head(const void* x, int M, const void* W, const float* w_scale, int V, int H, int wfmt, float* logits,

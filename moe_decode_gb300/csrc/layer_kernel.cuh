@@ -607,13 +607,17 @@ __device__ __forceinline__ void decode_block(const uint4 q, uint32_t (&w)[16]) {
     w[12] = t[0], w[13] = t[1], w[14] = t[2], w[15] = t[3];
 }
 
-// MXFP4 gate and up rows against tokens held in f16 (times their power of
-// two, which the caller removes).
+// MXFP4 gate and up rows against tokens held in f16 times 2^s_t. The
+// token's 2^-s_t (xi[t]) is folded into each block's e8m0 scale: a product
+// of two powers of two is exact, so the result is what removing 2^s_t at the
+// end would give, but an extreme block scale (up to 2^127) cannot overflow
+// the sum of scaled tokens when the true sum is finite.
 template <int NT>
 __device__ __forceinline__ void dot2_mxh(const uint4* __restrict__ c1, const uint8_t* __restrict__ s1,
                                          const uint4* __restrict__ c3, const uint8_t* __restrict__ s3,
-                                         const uint4* __restrict__ x0, const uint4* __restrict__ x1, int nblk,
-                                         int lane, float (&g)[NT], float (&u)[NT]) {
+                                         const uint4* __restrict__ x0, const uint4* __restrict__ x1,
+                                         const float (&xi)[NT], int nblk, int lane, float (&g)[NT],
+                                         float (&u)[NT]) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) g[t] = u[t] = 0.f;
 #pragma unroll 2
@@ -627,8 +631,8 @@ __device__ __forceinline__ void dot2_mxh(const uint4* __restrict__ c1, const uin
         for (int t = 0; t < NT; ++t) {
             const uint4* xb = (t == 0 ? x0 : x1) + 4 * b;
             const uint4 a[4] = {xb[r], xb[1 ^ r], xb[2 ^ r], xb[3 ^ r]};
-            g[t] = fmaf(block_h(w1, a), sc1, g[t]);
-            u[t] = fmaf(block_h(w3, a), sc3, u[t]);
+            g[t] = fmaf(block_h(w1, a), sc1 * xi[t], g[t]);
+            u[t] = fmaf(block_h(w3, a), sc3 * xi[t], u[t]);
         }
     }
 }
@@ -854,8 +858,12 @@ struct Consumer {
             const uint4* c3 = reinterpret_cast<const uint4*>(st + (ch.n + j) * cb);
             const uint8_t* s1 = st + 2 * ch.n * cb + j * sbytes;
             const uint8_t* s3 = st + 2 * ch.n * cb + (ch.n + j) * sbytes;
-            if (WFMT == 1)
-                dot2_mxh<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), p.H / 32, lane, g, u);
+            if (WFMT == 1) {
+                float xi[NT];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) xi[t] = plan->x_inv[t == 0 ? t0tok : t1tok];
+                dot2_mxh<NT>(c1, s1, c3, s3, xrow(t0tok), xrow(t1tok), xi, p.H / 32, lane, g, u);
+            }
             else
                 dot2_fp8<NT>(c1, reinterpret_cast<const float*>(s1), c3, reinterpret_cast<const float*>(s3),
                              xrow(t0tok), xrow(t1tok), p.H / 16, lane, g, u);
@@ -888,8 +896,9 @@ struct Consumer {
                 float gs = warp_sum4(g[0], u[0], g[1], u[1], lane);
                 float us = __shfl_down_sync(0xffffffffu, gs, 8);
                 if ((lane & 15) == 0) {
-                    // f16 tokens are held times 2^s_t (MXFP4)
-                    if (TWO ? !shared : WFMT == 1) {
+                    // f16 tokens are held times 2^s_t (MXFP4); the routed
+                    // MXFP4 dot removes it block by block
+                    if (WFMT == 1 && shared && !TWO) {
                         const float xi = plan->x_inv[lane ? tb : ta];
                         gs *= xi, us *= xi;
                     }
@@ -903,7 +912,7 @@ struct Consumer {
                 float gs = warp_sum2(g[0], u[0], lane);
                 float us = __shfl_down_sync(0xffffffffu, gs, 16);
                 if (lane == 0) {
-                    if (TWO ? !shared : WFMT == 1) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
+                    if (WFMT == 1 && shared && !TWO) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
                     hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(gs, us));
                 }
             }
@@ -1065,10 +1074,14 @@ __device__ __forceinline__ float key_f32(uint32_t k) {
 // and rescans. The code stays small on purpose: it runs once per launch, so
 // its instructions are fetched cold. Returns false when the wait ran out
 // (the CTA is then aborted).
-template <int EPL, bool VAR>
+// PUBNUM (split-K one-token layer): each published slot also carries its
+// unnormalised weight (exp(l_j - l_max), or the score s_j), and the final
+// factor routed_scale / sum is published once all k rounds are done.
+template <int EPL, bool VAR, bool PUBNUM = false>
 __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lrow, const int E, const int k,
                                        int lane, uint32_t tag, const LayerParams& p, Plan* plan,
-                                       int32_t* __restrict__ sel_e, float* __restrict__ sel_w, bool publish) {
+                                       const float* __restrict__ bias, int32_t* __restrict__ sel_e,
+                                       float* __restrict__ sel_w, bool publish) {
     float lg[EPL];
     uint64_t t0 = 0;
     for (int spin = 0;; ++spin) {
@@ -1130,7 +1143,7 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
     for (int j = 0; j < EPL; ++j) {
         const uint32_t e = idx_of(j);
         float kv = sc[j];
-        if (!by_logit && p.bias && e < (uint32_t)E) kv += __ldg(p.bias + e);
+        if (!by_logit && bias && e < (uint32_t)E) kv += bias[e];
         key[j] = e < (uint32_t)E ? f32_key(kv) : 0u;
     }
     uint32_t bk = 0u, bi = 0xffffffffu;
@@ -1147,7 +1160,7 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
         float ws = 0.f;
         if (lane == 0) {
             sel_e[jj] = (int32_t)we;
-            if (publish) {  // slot jj is the jj-th selected expert: its tiles may stream now
+            if (publish && !PUBNUM) {  // slot jj is the jj-th selected expert: its tiles may stream now
                 plan->slot_e[jj] = (int16_t)we;
                 st_release_cta(&plan->known, jj + 1);
             }
@@ -1173,17 +1186,23 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
             ws = __shfl_sync(0xffffffffu, ws, (int)((we & 63u) >> 1));  // from the winning lane
         if (jj == 0) first = ws;
         if (lane == jj) mine = ws;
+        if (PUBNUM && lane == 0) {  // the slot and its unnormalised weight
+            plan->slot_e[jj] = (int16_t)we;
+            plan->slot_num[jj] = by_logit ? expf(ws - first) : ws;
+            st_release_cta(&plan->known, jj + 1);
+        }
     }
     const float num = lane < k ? (by_logit ? expf(mine - first) : mine) : 0.f;
     float den = num;
 #pragma unroll
     for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (lane < k) sel_w[lane] = num / den * p.routed_scale;
+    if (PUBNUM && lane == 0) plan->wscale = p.routed_scale / den;
     return true;
 }
 
-static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* plan, int warp, int lane,
-                                                   int nwarps, bool publish) {
+static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* plan, const float* bias, int warp,
+                                                   int lane, int nwarps, bool publish) {
     // the debug hook waits for a tag that never comes
     const uint32_t tag = plan->tag + (p.force_timeout ? 1u : 0u);
     for (int t = warp; t < p.M; t += nwarps) {
@@ -1194,11 +1213,11 @@ static __device__ __forceinline__ void topk_tokens(const LayerParams& p, Plan* p
         bool ok;
         const bool pub = publish && t == 0;
         if (p.E <= 512)
-            ok = var ? topk_warp<16, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub)
-                     : topk_warp<16, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub);
+            ok = var ? topk_warp<16, true>(lrow, p.E, p.k, lane, tag, p, plan, bias, se, sw, pub)
+                     : topk_warp<16, false>(lrow, p.E, p.k, lane, tag, p, plan, bias, se, sw, pub);
         else
-            ok = var ? topk_warp<32, true>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub)
-                     : topk_warp<32, false>(lrow, p.E, p.k, lane, tag, p, plan, se, sw, pub);
+            ok = var ? topk_warp<32, true>(lrow, p.E, p.k, lane, tag, p, plan, bias, se, sw, pub)
+                     : topk_warp<32, false>(lrow, p.E, p.k, lane, tag, p, plan, bias, se, sw, pub);
         if (!ok) return;
     }
 }
@@ -1470,8 +1489,19 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         constexpr bool TWO = ONE && WFMT == 1;
         Consumer<WFMT, TWO> cs{p, plan, ring0, xs, reinterpret_cast<const uint16_t*>(smem + p.off_xb), ypair,
                                warp, lane, 0, h0};
+        const float* bias_s = p.bias ? reinterpret_cast<const float*>(smem + p.off_bias) : nullptr;
+        // The router's selection bias is a model parameter, not an output of
+        // the previous launch: it is staged before the dependency wait.
+        if (p.bias)
+            for (int i = tid; i < p.E; i += NCT) const_cast<float*>(bias_s)[i] = __ldg(p.bias + i);
         pdl_wait();
-        if (tid == 0) plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
+        if (tid == 0) {
+            plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
+            // a call that ran out of time left the control words stale: every
+            // later call on this workspace refuses to run until it is zeroed
+            if ((int)ld_acquire_gpu(p.ctrl + kCtlStatus) == -101 /* MOE_ETIMEOUT */)
+                set_abort(p, plan, -101);
+        }
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
@@ -1548,7 +1578,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                     plan->npairs = p.k;
                 }
                 __syncwarp();
-                if (!aborted(plan)) topk_tokens(p, plan, warp, lane, 1, true);
+                if (!aborted(plan)) topk_tokens(p, plan, bias_s, warp, lane, 1, true);
                 if (tid == 0) trace_mark(p, 4);
                 __syncwarp();
                 if (lane < p.k && !aborted(plan)) {
@@ -1568,7 +1598,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             ok = cs.consume_phase();
             if (tid == 0) trace_mark(p, 2);
             // no grid barrier: each token's warp waits for the tagged logits
-            if (!aborted(plan)) topk_tokens(p, plan, warp, lane, NCW, false);
+            if (!aborted(plan)) topk_tokens(p, plan, bias_s, warp, lane, NCW, false);
             if (tid == 0) trace_mark(p, 4);
             named_bar_sync(1, NCT);
             if (cta == 0 && !aborted(plan)) {

@@ -16,6 +16,7 @@ constexpr int kMaxM = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
+constexpr int kMaxGrid = 256;  // CTAs of a split-K layer launch (workspace sizing)
 
 // workspace control block (uint32 words, 128 bytes apart): status, launch
 // epoch (advanced by the last CTA of every call), grid barrier, exit counter,
@@ -41,6 +42,9 @@ struct LayerParams {
     const uint16_t* ws1;   // shared expert, bf16
     const uint16_t* ws3;
     const uint16_t* ws2;
+    const uint16_t* w2t;   // optional down projections transposed, bf16 [E, I, H]
+    const uint16_t* ws2t;  // and the shared expert's, [Is, H] (split-K layer)
+    float* ypart;          // split-K layer: per-CTA partial outputs [G, H] fp32
     const int32_t* idx_in; // FFN mode routing
     const float* w_in;
     int32_t* idx_out;      // may be null
@@ -70,7 +74,8 @@ struct LayerParams {
     // shared-memory offsets: barriers, plan, tokens, a second copy of the
     // tokens in plain bf16 (one-token MXFP4 launches; otherwise the same
     // buffer), per-pair down results
-    uint32_t off_bar, off_plan, off_x, off_xb, off_yacc, smem_bytes;
+    // router selection bias staged from p.bias (only when p.bias is set)
+    uint32_t off_bar, off_plan, off_x, off_xb, off_yacc, off_bias, smem_bytes;
 };
 
 // A unit of the ring: the tiles one stage holds. kind 0 router rows, 1
@@ -99,6 +104,9 @@ struct Plan {
     int16_t slot_p0[kMaxEntries + 1];
     int16_t order[kMaxK];           // M = 1: its pairs by ascending expert (combine order)
     int32_t known;                  // M = 1: slots whose expert is known so far
+    float slot_num[kMaxK];          // split-K layer: unnormalised routing weight of
+                                    // each slot, published with the slot
+    float wscale;                   // split-K layer: routed_scale / sum of slot_num
     float x_inv[kMaxM];             // MXFP4 layers: tokens are held in f16 times
                                     // 2^s_t; x_inv[t] = 2^-s_t
     int32_t nslot;

@@ -34,7 +34,12 @@ def build(force: bool = False) -> str:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
                "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
-        subprocess.check_call(cmd)
+        # OpenMP only spreads oracle_ffn_parallel's independent expert calls
+        # over threads; without it that function runs on one thread
+        try:
+            subprocess.check_call(cmd[:1] + ["-fopenmp"] + cmd[1:], stderr=subprocess.DEVNULL)
+        except (subprocess.CalledProcessError, OSError):
+            subprocess.check_call(cmd)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -63,7 +68,11 @@ def _load():
         lib.oracle_expert.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, i32, P]
         lib.oracle_ffn.argtypes = [P, i32, i32, P, P, i32, i32, i32, i32,
                                    P, P, P, P, P, P, i32, P, P, P, i32, P]
-        for f in ("oracle_mxfp4_decode", "oracle_route", "oracle_expert", "oracle_ffn"):
+        lib.oracle_ffn_parallel.argtypes = [P, i32, i32, P, P, i32, i32, i32, i32,
+                                            P, P, P, P, P, P, i32, P, P, P, i32, i32, P]
+        lib.oracle_threads.argtypes = []
+        for f in ("oracle_mxfp4_decode", "oracle_route", "oracle_expert", "oracle_ffn", "oracle_ffn_parallel",
+                  "oracle_threads"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -150,14 +159,21 @@ def expert(x_f32: np.ndarray, W1, W3, W2, wfmt: int = 0, S=(None, None, None),
     return z
 
 
+def threads() -> int:
+    """Host threads oracle_ffn_parallel may use (1 if built without OpenMP)."""
+    return int(_load().oracle_threads())
+
+
 def ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict, E: int, I: int,
-        shared=None, wfmt: int = 0, acc_double: bool = False) -> np.ndarray:
+        shared=None, wfmt: int = 0, acc_double: bool = False, nthreads: int = 1) -> np.ndarray:
     """Expert FFN with given routing.
 
     experts maps expert id -> (W1, W3, W2) for bf16, or
     (W1q, S1, W3q, S3, W2q, S2) for MXFP4 (u8 scales) and FP8 (fp32 scales
     per 128 elements); only the ids present in idx are
     needed. shared is (Ws1, Ws3, Ws2) bf16 or None. Returns y fp32 [M, H].
+    nthreads != 1 runs the expert calls on that many host threads (0: all),
+    with a bit-identical result.
     """
     x = _c(x, np.uint16)
     M, H = x.shape
@@ -184,9 +200,15 @@ def ffn(x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts: dict, E: int, I:
         Ws = tuple(_c(m, np.uint16) for m in shared)
         Is = Ws[0].shape[0]
     y = np.empty((M, H), dtype=np.float32)
-    rc = _load().oracle_ffn(_ptr(x), M, H, _ptr(idx), _ptr(w), k, E, I, wfmt,
-                            arr["W1"], arr["S1"], arr["W3"], arr["S3"], arr["W2"], arr["S2"],
-                            Is, _ptr(Ws[0]), _ptr(Ws[1]), _ptr(Ws[2]), int(acc_double), _ptr(y))
+    if nthreads != 1:
+        rc = _load().oracle_ffn_parallel(_ptr(x), M, H, _ptr(idx), _ptr(w), k, E, I, wfmt,
+                                         arr["W1"], arr["S1"], arr["W3"], arr["S3"], arr["W2"], arr["S2"],
+                                         Is, _ptr(Ws[0]), _ptr(Ws[1]), _ptr(Ws[2]), int(acc_double), nthreads,
+                                         _ptr(y))
+    else:
+        rc = _load().oracle_ffn(_ptr(x), M, H, _ptr(idx), _ptr(w), k, E, I, wfmt,
+                                arr["W1"], arr["S1"], arr["W3"], arr["S3"], arr["W2"], arr["S2"],
+                                Is, _ptr(Ws[0]), _ptr(Ws[1]), _ptr(Ws[2]), int(acc_double), _ptr(y))
     if rc:
         raise ValueError(f"oracle_ffn rc={rc}")
     return y

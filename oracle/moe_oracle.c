@@ -13,6 +13,9 @@
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 float oracle_bf16_to_f32(uint16_t b) {
     uint32_t u = (uint32_t)b << 16;
@@ -273,6 +276,83 @@ int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
     }
     free(xt); free(z); free(acc);
     return rc;
+}
+
+/* The same FFN with the work spread over host threads, for the timed CPU
+ * baseline: the (token, selected expert) pairs and each token's shared expert
+ * are independent oracle_expert calls, run by an OpenMP parallel loop
+ * (nthreads threads, 0: all); their outputs are then combined exactly as
+ * oracle_ffn combines them (same order, same arithmetic), so y is
+ * bit-identical to oracle_ffn's. Without OpenMP the loop runs on one thread. */
+int oracle_ffn_parallel(const uint16_t* x, int M, int H, const int32_t* idx,
+                        const float* w, int k, int E, int I, int wfmt,
+                        const void* const* W1, const uint8_t* const* S1,
+                        const void* const* W3, const uint8_t* const* S3,
+                        const void* const* W2, const uint8_t* const* S2,
+                        int Is, const uint16_t* Ws1, const uint16_t* Ws3,
+                        const uint16_t* Ws2, int acc_double, int nthreads, float* y) {
+    if (!x || !y || M < 0 || H <= 0 || k < 0 || E <= 0 || I <= 0 || Is < 0) return -1;
+    if (k > 0 && (!idx || !w || !W1 || !W3 || !W2)) return -1;
+    if (wfmt != 0 && k > 0 && (!S1 || !S3 || !S2)) return -1;
+    if (Is > 0 && (!Ws1 || !Ws3 || !Ws2)) return -1;
+    const int per = k + (Is > 0 ? 1 : 0);
+    const int ntask = M * per;
+    float* xf = (float*)malloc(sizeof(float) * (size_t)M * H + 1);
+    float* z = (float*)malloc(sizeof(float) * (size_t)ntask * H + 1);
+    int* rcs = (int*)calloc((size_t)ntask + 1, sizeof(int));
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!xf || !z || !rcs || !acc) { free(xf); free(z); free(rcs); free(acc); return -2; }
+    for (int64_t i = 0; i < (int64_t)M * H; ++i) xf[i] = oracle_bf16_to_f32(x[i]);
+    int nt = nthreads;
+#ifdef _OPENMP
+    if (nt <= 0) nt = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+    for (int q = 0; q < ntask; ++q) {
+        const int t = q / per, j = q % per;
+        const float* xt = xf + (int64_t)t * H;
+        float* zq = z + (int64_t)q * H;
+        if (j < k) {
+            const int e = idx[(int64_t)t * k + j];
+            if (e < 0 || e >= E || !W1[e] || !W3[e] || !W2[e]) { rcs[q] = -3; continue; }
+            const uint8_t *a = NULL, *b = NULL, *d = NULL;
+            if (wfmt != 0) { a = S1[e]; b = S3[e]; d = S2[e]; }
+            rcs[q] = oracle_expert(xt, H, I, wfmt, W1[e], a, W3[e], b, W2[e], d, acc_double, zq);
+        } else {
+            rcs[q] = oracle_expert(xt, H, Is, 0, Ws1, NULL, Ws3, NULL, Ws2, NULL, acc_double, zq);
+        }
+    }
+    (void)nt;
+    int rc = 0;
+    for (int q = 0; q < ntask && rc == 0; ++q) rc = rcs[q];
+    for (int t = 0; t < M && rc == 0; ++t) {
+        for (int c = 0; c < H; ++c) acc[c] = 0.0;
+        for (int j = 0; j < per; ++j) {
+            const float* zq = z + ((int64_t)t * per + j) * H;
+            const float wj = j < k ? w[(int64_t)t * k + j] : 1.0f;
+            for (int c = 0; c < H; ++c) {
+                if (j < k) {
+                    if (acc_double) acc[c] += (double)wj * (double)zq[c];
+                    else acc[c] = (double)((float)acc[c] + wj * zq[c]);
+                } else {
+                    if (acc_double) acc[c] += (double)zq[c];
+                    else acc[c] = (double)((float)acc[c] + zq[c]);
+                }
+            }
+        }
+        for (int c = 0; c < H; ++c) y[(int64_t)t * H + c] = (float)acc[c];
+    }
+    free(xf); free(z); free(rcs); free(acc);
+    return rc;
+}
+
+/* Threads an OpenMP parallel region may use here (1 without OpenMP). */
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }
 
 /* ------------------------------------------------------------------ FP8 */

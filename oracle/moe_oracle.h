@@ -118,6 +118,21 @@ int oracle_ffn(const uint16_t* x, int M, int H, const int32_t* idx,
                int Is, const uint16_t* Ws1, const uint16_t* Ws3,
                const uint16_t* Ws2, int acc_double, float* y);
 
+/* oracle_ffn computed by nthreads host threads (OpenMP over the (token,
+ * selected expert) pairs and the shared expert; 0: all threads), combined in
+ * oracle_ffn's order: y is bit-identical to oracle_ffn's. For the timed
+ * all-core CPU baseline. */
+int oracle_ffn_parallel(const uint16_t* x, int M, int H, const int32_t* idx,
+                        const float* w, int k, int E, int I, int wfmt,
+                        const void* const* W1, const uint8_t* const* S1,
+                        const void* const* W3, const uint8_t* const* S3,
+                        const void* const* W2, const uint8_t* const* S2,
+                        int Is, const uint16_t* Ws1, const uint16_t* Ws3,
+                        const uint16_t* Ws2, int acc_double, int nthreads, float* y);
+
+/* Host threads available to oracle_ffn_parallel (1 without OpenMP). */
+int oracle_threads(void);
+
 #ifdef __cplusplus
 }
 #endif

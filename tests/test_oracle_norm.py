@@ -51,6 +51,41 @@ def test_matches_an_independent_float64_computation(oracle):
     hf = oracle.bf16_to_f32(h).astype(np.float64)
     gf = oracle.bf16_to_f32(gamma).astype(np.float64)
     v = hf / np.sqrt((hf * hf).mean(axis=1, keepdims=True) + 1e-6) * gf
-    b = v.astype(np.float32).view(np.uint32).astype(np.uint64)
-    want = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+    # nearest bf16 of each float64 value, found from its two bf16 neighbours
+    # (no intermediate float32 rounding): the neighbour below in magnitude is
+    # the float64 value truncated to 8 significant bits
+    a = np.abs(v)
+    e = np.floor(np.log2(a))
+    ulp = np.exp2(e - 7)
+    lo = np.floor(a / ulp) * ulp
+    hi = lo + ulp
+    lo_bits = oracle_bits(lo)
+    pick_hi = (hi - a < a - lo) | ((hi - a == a - lo) & ((lo_bits & 1) == 1))
+    mag = np.where(pick_hi, oracle_bits(hi), lo_bits)
+    want = (mag | np.where(v < 0, 0x8000, 0)).astype(np.uint16)
     assert np.array_equal(oracle.rmsnorm(h, gamma, 1e-6), want)
+
+
+def oracle_bits(a):
+    """bf16 bit patterns of float64 values that are exactly bf16 values."""
+    f = np.asarray(a, np.float64).astype(np.float32)
+    assert np.array_equal(f.astype(np.float64), np.asarray(a, np.float64))
+    return (f.view(np.uint32) >> 16).astype(np.uint32)
+
+
+def test_rounding_ties_go_to_even_both_ways(oracle):
+    """Hand-built exact ties. h = (3, 3, 3, 1, 1, 1, 1, 1) has mean square 4,
+    so 1 / rms = 0.5 exactly and x_i = h_i * 0.5 * g_i without rounding
+    before the final cast. With g = 1 + 2^-7, x_0 = 1.51171875 lies exactly
+    halfway between the bf16 neighbours 1.5078125 (odd mantissa 65) and
+    1.515625 (even, 66): nearest-even rounds up. With g = 1 + 3 * 2^-7,
+    x_1 = 1.53515625 lies halfway between 1.53125 (even, 68) and 1.5390625
+    (odd, 69): nearest-even rounds down, where rounding half up would not.
+    x_2 is the negative of x_0's tie. The rest are exact (0.5)."""
+    h = np.array([[0x4040, 0x4040, 0x4040, 0x3F80, 0x3F80, 0x3F80, 0x3F80, 0x3F80]], np.uint16)
+    gamma = np.array([0x3F81, 0x3F83, 0xBF81, 0x3F80, 0x3F80, 0x3F80, 0x3F80, 0x3F80], np.uint16)
+    want = np.array([0x3FC2, 0x3FC4, 0xBFC2, 0x3F00, 0x3F00, 0x3F00, 0x3F00, 0x3F00], np.uint16)
+    got = oracle.rmsnorm(h, gamma, 0.0)[0]
+    assert np.array_equal(got, want), [hex(v) for v in got]
+    # the same values just off the tie round to the nearer neighbour
+    assert oracle.bf16_to_f32(want[:2]).tolist() == [1.515625, 1.53125]

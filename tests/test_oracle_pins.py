@@ -327,3 +327,35 @@ def test_ling_single_token_fp32_vs_fp64(oracle):
     y32 = oracle.ffn(x, idx, w, experts, 512, 768, shared)
     y64 = oracle.ffn(x, idx, w, experts, 512, 768, shared, acc_double=True)
     assert np.linalg.norm(y32 - y64) / np.linalg.norm(y64) < 1e-5
+
+
+# ---------------------------------------------------------------- all-core variant
+
+@pytest.mark.parametrize("wfmt,shared", [(0, True), (0, False), (1, True), (2, True)])
+def test_parallel_ffn_is_bit_identical(oracle, wfmt, shared):
+    """The threaded FFN used for the all-core CPU baseline runs the same
+    expert calls and combines them in the same order: the same bits as the
+    single-thread oracle, for every weight format."""
+    sh = synth.LayerShape(512, 16, 3, 128, 128) if wfmt == 2 else synth.LayerShape(256, 16, 3, 64, 64)
+    layer = synth.device_layer(sh, 2, wfmt=wfmt, device="cpu")
+    x = synth.to_u16(synth.x_independent(sh, 3, 5))
+    idx, w, _ = oracle.route(x, synth.to_u16(layer["Wg"]), sh.top_k)
+    experts = {int(e): synth.host_expert(sh, layer, int(e), wfmt) for e in np.unique(idx)}
+    sw = tuple(synth.to_u16(layer[n]) for n in ("ws1", "ws3", "ws2")) if shared else None
+    y1 = oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, sw, wfmt=wfmt)
+    for nt in (0, 2, 3):
+        yp = oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, sw, wfmt=wfmt, nthreads=nt)
+        assert np.array_equal(y1.view(np.uint32), yp.view(np.uint32))
+    yd = oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, sw, wfmt=wfmt, acc_double=True)
+    ydp = oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, sw, wfmt=wfmt, acc_double=True, nthreads=0)
+    assert np.array_equal(yd.view(np.uint32), ydp.view(np.uint32))
+
+
+def test_parallel_ffn_rejects_a_missing_expert(oracle):
+    sh = synth.TINY
+    x = synth.to_u16(synth.x_independent(sh, 4, 2))
+    idx = np.array([[1, 2], [3, 4]], np.int32)
+    w = np.full((2, 2), 0.5, np.float32)
+    experts = {e: tuple(synth.to_u16(m) for m in synth.expert_weights(sh, 0, e)) for e in (1, 2, 3)}
+    with pytest.raises(ValueError):
+        oracle.ffn(x, idx, w, experts, sh.n_experts, sh.inter, None, nthreads=0)

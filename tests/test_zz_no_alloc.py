@@ -36,7 +36,7 @@ def test_rejects_shapes_beyond_the_static_scratch(api):
     ling = api.make_shape(2560, 512, 8, 768, 768, 0)
     assert api.workspace_bytes(ling, 16) <= api.STATIC_SCRATCH_BYTES
     assert api.lib.moe_decode_layer_static_scratch(fake, 1, fake, ctypes.byref(w), ctypes.byref(ling), None, None,
-                                                   fake, 1 << 8, None) == api.EINVAL   # flag not accepted here
+                                                   fake, 1 << 4, None) == api.EINVAL   # unknown flag
 
 
 def _run_pair(api, layer, shape, wfmt, x, flags=0):
@@ -62,7 +62,7 @@ def _run_pair(api, layer, shape, wfmt, x, flags=0):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("wfmt", [0, 1])
+@pytest.mark.parametrize("wfmt", [0, 1, 2])
 def test_matches_decode_layer_on_two_calls_in_a_row(api, wfmt):
     api.set_option(api.OPT_GRID_CTAS, 0)
     api.set_option(api.OPT_WAIT_TIMEOUT_NS, 1_000_000_000)
@@ -101,3 +101,34 @@ def test_allocates_nothing_and_resets(api):
     assert torch.equal(y_static, y_ref)
     (_, _, y_ref2), _ = _run_pair(api, layer, sh, 0, xs[2])
     assert torch.equal(ys[2], y_ref2)
+
+
+@pytest.mark.gpu
+def test_timeout_is_reported_sticky_and_cleared_by_reset(api):
+    """A bounded device wait forced to run out (a 2 ms budget) is reported
+    through moe_static_scratch_status; the next plain call refuses to run
+    (its output stays untouched and the status stays MOE_ETIMEOUT) instead of
+    computing on stale control words; a call with MOE_F_RESET_SCRATCH then
+    matches moe_decode_layer bit for bit."""
+    from parity_util import expert_weights_of
+    api.set_option(api.OPT_GRID_CTAS, 0)
+    sh = synth.TINY
+    layer = synth.device_layer(sh, 0)
+    ew = expert_weights_of(layer, 0)
+    s = api.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.inter, sh.shared_inter, 0)
+    x = synth.x_independent(sh, 70, 3, device="cuda")
+    y = torch.zeros((3, sh.hidden), dtype=torch.bfloat16, device="cuda")
+    api.set_option(api.OPT_WAIT_TIMEOUT_NS, 2_000_000)
+    try:
+        api.decode_layer_static_scratch(x, layer["Wg"], ew, s, y, flags=api.F_DEBUG_FORCE_TIMEOUT)
+        assert api.static_scratch_status() == api.ETIMEOUT
+    finally:
+        api.set_option(api.OPT_WAIT_TIMEOUT_NS, 1_000_000_000)
+    y_stale = torch.full_like(y, 7.0)
+    api.decode_layer_static_scratch(x, layer["Wg"], ew, s, y_stale)
+    assert api.static_scratch_status() == api.ETIMEOUT
+    assert torch.equal(y_stale, torch.full_like(y, 7.0))
+    api.decode_layer_static_scratch(x, layer["Wg"], ew, s, y, flags=api.F_RESET_SCRATCH)
+    assert api.static_scratch_status() == 0
+    (_, _, y_ref), _ = _run_pair(api, layer, sh, 0, x)
+    assert torch.equal(y, y_ref)
