@@ -40,8 +40,14 @@ PERIOD = 64  # input ring length; the copy rotation divides it
 # copies: layer copies rotated per step. The full-size workloads use at least
 # as many as the cold-weight rule needs (see cold_copies); the small profiling
 # cases keep a fixed, small count.
+# down_t: the layer is given its down projections also transposed (made once
+# at load time with moe_transpose_down), which one-token calls use to split the
+# down projection along the intermediate dimension (no grid barrier between
+# the gate/up and down projections; measured slower than the two-phase layer
+# at the Ling shape, reported beside it)
 WORKLOADS = {
     "ling_m1": dict(M=1, wfmt=0, copies=4, gen="independent"),
+    "ling_m1_splitk": dict(M=1, wfmt=0, copies=4, gen="independent", down_t=True),
     "ling_m6": dict(M=6, wfmt=0, copies=4, gen="independent"),
     "ling_m10": dict(M=10, wfmt=0, copies=4, gen="overlap"),
     "mxfp4_m1": dict(M=1, wfmt=1, copies=8, gen="independent"),
@@ -51,6 +57,7 @@ WORKLOADS = {
     # small cases for detailed profiler captures: the Ling layer cut to 128
     # experts (1.5 GB per copy), still far above L2
     "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128, fixed_copies=True),
+    "ling_e128_m1_splitk": dict(M=1, wfmt=0, copies=2, gen="independent", E=128, fixed_copies=True, down_t=True),
     "ling_e128_m10": dict(M=10, wfmt=0, copies=2, gen="overlap", E=128, fixed_copies=True),
     "mxfp4_e128_m6": dict(M=6, wfmt=1, copies=2, gen="independent", E=128, fixed_copies=True),
     "fp8_e128_m6": dict(M=6, wfmt=2, copies=2, gen="independent", E=128, fixed_copies=True),
@@ -111,6 +118,8 @@ def describe(name: str, copies: int) -> str:
     E = w.get("E", 512)
     fmt = {0: "bf16", 1: "MXFP4 (e2m1 + e8m0/32) routed experts, bf16 router and shared expert",
            2: "FP8 (e4m3 + fp32 scale/128) routed experts, bf16 router and shared expert"}[w["wfmt"]]
+    if w.get("down_t"):
+        fmt += " (down projections given transposed: split-K one-token path)"
     gen = ("tokens drawn independently" if w["gen"] == "independent"
            else "tokens with ~50% consecutive top-8 overlap")
     return (f"Ling-shape MoE layer H=2560 E={E} top-8 I=768 shared I=768, {fmt}, M={w['M']} ({gen}), "
@@ -264,9 +273,21 @@ class Workload:
         self.shape = sh
         self.cshape = api.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.inter, sh.shared_inter, self.wfmt)
         self.layers = cache.get(sh, self.wfmt, self.ncopy, device)
+        self.down_t = bool(w.get("down_t"))
+        if self.down_t:
+            for L in self.layers:
+                if "w2t" not in L:  # kept with the cached copy for later workloads
+                    L["w2t"] = api.transpose_down(L["w2"])
+                    L["ws2t"] = api.transpose_down(L["ws2"])
+        used = ["Wg", "w1", "w3", "w2", "ws1", "ws3", "ws2", "s1", "s3", "s2"]
+        if self.down_t:
+            used = [n for n in used if n not in ("w2", "ws2")] + ["w2t", "ws2t"]
         self.weights = [api.ExpertWeights(w1=L["w1"], w3=L["w3"], w2=L["w2"], ws1=L["ws1"], ws3=L["ws3"],
-                                          ws2=L["ws2"], s1=L.get("s1"), s3=L.get("s3"), s2=L.get("s2"))
+                                          ws2=L["ws2"], s1=L.get("s1"), s3=L.get("s3"), s2=L.get("s2"),
+                                          w2t=L.get("w2t") if self.down_t else None,
+                                          ws2t=L.get("ws2t") if self.down_t else None)
                         for L in self.layers]
+        self.used_keys = used
         self.cweights = [wt.cstruct() for wt in self.weights]
         gen = synth.x_independent if w["gen"] == "independent" else synth.x_overlap
         self.xs = torch.stack([gen(sh, s, self.M, device=device) for s in range(PERIOD)])
@@ -274,7 +295,8 @@ class Workload:
         self.y = torch.empty((self.M, sh.hidden), dtype=torch.bfloat16, device=device)
         self.idx = torch.empty((PERIOD, self.M, sh.top_k), dtype=torch.int32, device=device)
         self.wout = torch.empty((PERIOD, self.M, sh.top_k), dtype=torch.float32, device=device)
-        self.weight_bytes = sum(t.numel() * t.element_size() for L in self.layers for t in L.values())
+        self.weight_bytes = sum(L[n].numel() * L[n].element_size() for L in self.layers for n in self.used_keys
+                                if n in L)
 
     def step(self, s: int, stream, idx=None, w=None, x=None, y=None):
         c = s % self.ncopy
@@ -575,7 +597,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(WORKLOADS), default="ling_m1")
-    ap.add_argument("--also", default="ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,fp8_m1,fp8_m6,"
+    ap.add_argument("--also", default="ling_m1_splitk,ling_m6,ling_m10,mxfp4_m1,mxfp4_m6,fp8_m1,fp8_m6,"
                                       "lmhead_bf16_m1,lmhead_fp8_m1,lmhead_bf16_m6," + SWEEP,
                     help="comma-separated extra workloads measured in the same run ('' for none)")
     ap.add_argument("--cpu-steps", type=int, default=0,
@@ -666,7 +688,8 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = main_res["hbm_gbs"]
     w = WORKLOADS[args.workload]
-    traffic = traffic_record("moe_layer_kernel", args.workload)
+    kname = "moe_layer_splitk_kernel" if w.get("down_t") and w["M"] == 1 else "moe_layer_kernel"
+    traffic = traffic_record(kname, args.workload)
     tasks = w["M"] * (layer_shape(args.workload).top_k + 1)
     line = {
         "metric": METRIC,
@@ -685,7 +708,7 @@ def main():
         "hbm_gbs": round(achieved, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "kernel": "moe_layer_kernel", "traffic": traffic},
+                     "kernel": kname, "traffic": traffic},
         "cpu_baseline": {"value": round(main_res["cpu_us"], 1), "unit": "us/step", "cores": 1,
                          "kind": "oracle",
                          "sample": f"{main_res['cpu_steps']} steps of the same workload (same inputs, routing "

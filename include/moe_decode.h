@@ -153,10 +153,24 @@ typedef struct moe_weights {
     const void* ws1;    /* shared expert, bf16; NULL when Is == 0 */
     const void* ws3;
     const void* ws2;
+    /* Optional copies of the down projections transposed: w2t bf16 [E, I, H]
+     * (w2t[e, i, :] = w2[e, :, i]) and ws2t bf16 [Is, H] (NULL when Is == 0),
+     * made once at weight load with moe_transpose_down. When both are given
+     * (bf16 experts, H <= 5376), one-token moe_decode_layer calls split the down
+     * projection along I: the CTA that computes rows i of an expert's SwiGLU
+     * activation also streams rows i of w2t and keeps a partial output, and
+     * one fixed-order sum of the partials closes the layer, so no grid
+     * barrier separates the gate/up and down projections ("Chasing the
+     * Batch-1 Floor", "Two fusions and a retune": expert weights re-laid
+     * once at load time for the decode kernel). Other calls ignore them. */
+    const void* w2t;
+    const void* ws2t;
 } moe_weights;
 
 /* Bytes of workspace a call with this shape and M needs. 0 for a shape or M
- * the library rejects. */
+ * the library rejects. At M = 1 this includes the split-K layer's partial
+ * outputs (MOE_MAX_GRID x H fp32). */
+#define MOE_MAX_GRID 256
 size_t moe_workspace_bytes(const moe_shape* shape, int M);
 
 /* Zeroes the whole workspace (device, ws_bytes) on `stream`; needed once
@@ -210,6 +224,8 @@ int moe_decode_layer(const void* x, int M, const void* Wg,
  *    one stream (or otherwise serialised), also against other threads.
  *  - flags: MOE_F_NO_PDL, MOE_F_DEBUG_FORCE_TIMEOUT, MOE_F_RESET_SCRATCH
  *    (zeroes the scratch before the launch).
+ *  - The transposed down projections (w2t, ws2t) are not used: one-token
+ *    calls take the same path as moe_decode_layer without them.
  *  - Failure detection: the device status word lives in the scratch; read it
  *    with moe_static_scratch_status. After MOE_ETIMEOUT every later call
  *    refuses to run (it reports MOE_ETIMEOUT again and leaves its outputs
@@ -258,6 +274,14 @@ int moe_fp8_quantize(const void* w, int64_t rows, int K, int block,
  * e4m3(code) * scale[row, col / block] (all device). */
 int moe_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows,
                     int K, int block, float* out, void* stream);
+
+/* Transposed copy of down projections for the split-K one-token layer:
+ * w2 bf16 [n, H, I] -> w2t bf16 [n, I, H] with w2t[e, i, h] = w2[e, h, i]
+ * (n = E for the routed experts, n = 1 and I = Is for the shared expert).
+ * Both device, not overlapping. Not on the hot path: run it once when the
+ * weights are loaded. */
+int moe_transpose_down(const void* w2, int64_t n, int H, int I, void* w2t,
+                       void* stream);
 
 /* Synchronises `stream`, then copies the device status word of `ws` to
  * *dev_status (MOE_OK or a device code above). Not for the hot path. */

@@ -46,7 +46,8 @@ class Shape(ctypes.Structure):
 
 
 class _Weights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("w1", "w3", "w2", "s1", "s3", "s2", "ws1", "ws3", "ws2")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w1", "w3", "w2", "s1", "s3", "s2", "ws1", "ws3", "ws2", "w2t",
+                                                 "ws2t")]
 
 
 def _load():
@@ -73,10 +74,11 @@ def _load():
     lib.moe_lm_head.argtypes = [P, I32, P, P, I32, I32, I32, P, P, SZ, ctypes.c_uint32, P]
     lib.moe_fp8_quantize.argtypes = [P, I64, I32, I32, P, P, P]
     lib.moe_fp8_dequant.argtypes = [P, P, I64, I32, I32, P, P]
+    lib.moe_transpose_down.argtypes = [P, I64, I32, I32, P, P]
     lib.moe_last_launch_count.argtypes = []
     for f in ("moe_workspace_init", "moe_route", "moe_ffn", "moe_decode_layer", "moe_decode_layer_static_scratch",
               "moe_read_status", "moe_static_scratch_status", "moe_mxfp4_dequant", "moe_set_option", "moe_last_launch_count",
-              "moe_lm_head", "moe_fp8_quantize", "moe_fp8_dequant"):
+              "moe_lm_head", "moe_fp8_quantize", "moe_fp8_dequant", "moe_transpose_down"):
         getattr(lib, f).restype = I32
     return lib
 
@@ -129,10 +131,13 @@ class ExpertWeights:
     s1: Optional[torch.Tensor] = None
     s3: Optional[torch.Tensor] = None
     s2: Optional[torch.Tensor] = None
+    w2t: Optional[torch.Tensor] = None   # bf16 [E, I, H] (transpose_down(w2)); one-token split-K layer
+    ws2t: Optional[torch.Tensor] = None  # bf16 [Is, H]
 
     def cstruct(self) -> _Weights:
         return _Weights(*(None if t is None else t.data_ptr() for t in
-                          (self.w1, self.w3, self.w2, self.s1, self.s3, self.s2, self.ws1, self.ws3, self.ws2)))
+                          (self.w1, self.w3, self.w2, self.s1, self.s3, self.s2, self.ws1, self.ws3, self.ws2,
+                           self.w2t, self.ws2t)))
 
 
 def workspace_bytes(shape: Shape, M: int) -> int:
@@ -217,6 +222,17 @@ def fp8_quantize(w, block: int, codes, scales, stream=None):
     rows, K = w.shape
     _check(lib.moe_fp8_quantize(_ptr(w), rows, K, block, _ptr(codes), _ptr(scales), _stream(stream)),
            "moe_fp8_quantize")
+
+
+def transpose_down(w2: torch.Tensor, stream=None) -> torch.Tensor:
+    """Transposed copy of down projections (moe_transpose_down): bf16
+    [n, H, I] (or [H, I]) -> [n, I, H] (or [I, H]), for the split-K one-token
+    layer. Weight preparation, not the hot path."""
+    src = w2 if w2.dim() == 3 else w2.unsqueeze(0)
+    n, H, I = src.shape
+    out = torch.empty((n, I, H), dtype=w2.dtype, device=w2.device)
+    _check(lib.moe_transpose_down(_ptr(src), n, H, I, _ptr(out), _stream(stream)), "moe_transpose_down")
+    return out if w2.dim() == 3 else out[0]
 
 
 def fp8_dequant(codes, scales, block: int, out, stream=None):

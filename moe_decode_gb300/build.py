@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libmoe_decode.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "layer_bf16.cu", "layer_mxfp4.cu", "layer_fp8.cu", "lm_head.cu"]
+SOURCES = ["api.cu", "layer_bf16.cu", "layer_mxfp4.cu", "layer_fp8.cu", "layer_splitk.cu", "lm_head.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

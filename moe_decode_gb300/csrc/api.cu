@@ -3,6 +3,7 @@
 // every entry point are in include/moe_decode.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -110,10 +111,11 @@ int check_shape(const moe_shape* s, int M) {
 }
 
 struct WsLayout {
-    size_t logits, hs, hr, total;
+    size_t logits, hs, hr, ypart, total;
 };
 
-WsLayout ws_layout(const moe_shape* s, int M) {
+// splitk: the one-token split-K layer's per-CTA partial outputs follow
+WsLayout ws_layout(const moe_shape* s, int M, bool splitk) {
     WsLayout w;
     size_t off = moe::kCtlBytes;
     w.logits = off;
@@ -122,20 +124,32 @@ WsLayout ws_layout(const moe_shape* s, int M) {
     off = align_up(off + (size_t)M * s->shared_inter * 2, 256);
     w.hr = off;
     off = align_up(off + (size_t)M * s->top_k * s->inter * 2, 256);
+    w.ypart = off;
+    if (splitk) off = align_up(off + (size_t)MOE_MAX_GRID * s->hidden * 4, 256);
     w.total = off;
     return w;
 }
 
+// The split-K one-token layer: bf16 experts with both transposed down
+// projections given, H <= 5461.
+bool use_splitk(const moe_shape* s, int M, int mode, const moe_weights* W) {
+    // one unit row (gate, up and transposed down rows: 6 H bytes) must fit a
+    // ring stage
+    return M == 1 && mode == moe::kModeLayer && s->wfmt == 0 && W && W->w2t &&
+           (s->shared_inter == 0 || W->ws2t) && 6u * (uint32_t)s->hidden <= moe::kStageBytes;
+}
+
 // Grid, ring depth and shared-memory carve-up of one call.
-int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, LayerParams& p, DeviceInfo& dev) {
+int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, LayerParams& p, DeviceInfo& dev,
+              bool splitk = false) {
     int rc = device_info(&dev);
     if (rc) return rc;
     if (!ws) return MOE_EWORKSPACE;
     if (!aligned16(ws)) return MOE_EALIGN;
-    WsLayout wl = ws_layout(s, M);
+    WsLayout wl = ws_layout(s, M, splitk);
     if (ws_bytes < wl.total) return MOE_EWORKSPACE;
     int G = g_opt.grid_ctas > 0 ? g_opt.grid_ctas : dev.sms;
-    if (G > dev.sms) return MOE_EINVAL;
+    if (G > dev.sms || (splitk && G > MOE_MAX_GRID)) return MOE_EINVAL;
     p.M = M;
     p.H = s->hidden;
     p.E = s->n_experts;
@@ -159,6 +173,7 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.Es = (s->n_experts + 1) & ~1;
     p.hs = reinterpret_cast<uint16_t*>(base + wl.hs);
     p.hr = reinterpret_cast<uint16_t*>(base + wl.hr);
+    p.ypart = splitk ? reinterpret_cast<float*>(base + wl.ypart) : nullptr;
 
     const size_t other_plan = align_up(sizeof(moe::Plan), 128);
     // one-token MXFP4 layers keep two copies of the tokens: f16 for the
@@ -166,8 +181,10 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     const bool two = s->wfmt == 1 && M == 1 && mode == moe::kModeLayer;
     const size_t x_one = align_up((size_t)M * p.H * 2, 128);
     const size_t x_bytes = x_one * (two ? 2 : 1);
-    // down-projection results per (pair, output row): [M + M*k][rpc]
-    const size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
+    // down-projection results per (pair, output row): [M + M*k][rpc]; the
+    // split-K layer keeps its cross-warp sums there instead
+    size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
+    if (splitk) y_bytes = std::max(y_bytes, align_up((size_t)(2 * 10 * 4 + 12 * 32) * 4, 128));
     const size_t bar_bytes = 128;
     // the router's selection bias, staged before the dependency wait
     const size_t bias_bytes = s->router_bias ? align_up((size_t)s->n_experts * 4, 128) : 0;
@@ -195,7 +212,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
 
 int launch(const LayerParams& p, int wfmt, cudaStream_t st, bool pdl, DeviceInfo& dev) {
     bool coop = dev.coop;
-    cudaError_t err = wfmt == 1   ? moe::launch_layer_mxfp4(p, st, pdl, coop)
+    cudaError_t err = p.ypart     ? moe::launch_layer_splitk(p, st, pdl, coop)
+                      : wfmt == 1 ? moe::launch_layer_mxfp4(p, st, pdl, coop)
                       : wfmt == 2 ? moe::launch_layer_fp8(p, st, pdl, coop)
                                   : moe::launch_layer_bf16(p, st, pdl, coop);
     if (err != cudaSuccess) {
@@ -214,7 +232,7 @@ bool weights_ok(const moe_weights* W, const moe_shape* s) {
 }
 
 bool weights_aligned(const moe_weights* W, const moe_shape* s) {
-    bool ok = aligned16(W->w1) && aligned16(W->w3) && aligned16(W->w2);
+    bool ok = aligned16(W->w1) && aligned16(W->w3) && aligned16(W->w2) && aligned16(W->w2t) && aligned16(W->ws2t);
     if (s->wfmt != 0) ok = ok && aligned16(W->s1) && aligned16(W->s3) && aligned16(W->s2);
     if (s->shared_inter > 0) ok = ok && aligned16(W->ws1) && aligned16(W->ws3) && aligned16(W->ws2);
     return ok;
@@ -230,6 +248,8 @@ void set_weights(LayerParams& p, const moe_weights* W) {
     p.ws1 = static_cast<const uint16_t*>(W->ws1);
     p.ws3 = static_cast<const uint16_t*>(W->ws3);
     p.ws2 = static_cast<const uint16_t*>(W->ws2);
+    p.w2t = static_cast<const uint16_t*>(W->w2t);
+    p.ws2t = static_cast<const uint16_t*>(W->ws2t);
 }
 
 }  // namespace
@@ -238,7 +258,7 @@ extern "C" {
 
 size_t moe_workspace_bytes(const moe_shape* shape, int M) {
     if (check_shape(shape, M) != MOE_OK) return 0;
-    return ws_layout(shape, M).total;
+    return ws_layout(shape, M, M == 1).total;
 }
 
 int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -299,7 +319,7 @@ int moe_decode_layer(const void* x, int M, const void* Wg, const moe_weights* we
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(y) || !weights_aligned(weights, shape)) return MOE_EALIGN;
     LayerParams p = {};
     DeviceInfo dev;
-    rc = configure(shape, M, moe::kModeLayer, ws, ws_bytes, p, dev);
+    rc = configure(shape, M, moe::kModeLayer, ws, ws_bytes, p, dev, use_splitk(shape, M, moe::kModeLayer, weights));
     if (rc) return rc;
     p.x = static_cast<const uint16_t*>(x);
     p.Wg = static_cast<const uint16_t*>(Wg);
@@ -318,7 +338,7 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     int rc = check_shape(shape, M);
     if (rc) return rc;
     if (flags & ~(MOE_F_NO_PDL | MOE_F_RESET_SCRATCH | MOE_F_DEBUG_FORCE_TIMEOUT)) return MOE_EINVAL;
-    if (ws_layout(shape, M).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ESCRATCH;
+    if (ws_layout(shape, M, false).total > MOE_STATIC_SCRATCH_BYTES) return MOE_ESCRATCH;
     if (!x || !Wg || !y || !weights_ok(weights, shape)) return MOE_EINVAL;
     if (!aligned16(x) || !aligned16(Wg) || !aligned16(y) || !weights_aligned(weights, shape)) return MOE_EALIGN;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -340,6 +360,7 @@ int moe_decode_layer_static_scratch(const void* x, int M, const void* Wg, const 
     p.y = static_cast<uint16_t*>(y);
     p.force_timeout = (flags & MOE_F_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
     set_weights(p, weights);
+    p.w2t = p.ws2t = nullptr;  // not used here (the classic path)
     return launch(p, shape->wfmt, st, (flags & MOE_F_NO_PDL) == 0, dev);
 }
 
@@ -422,6 +443,19 @@ int moe_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows, int
         return MOE_ECUDA;
     }
     g_last_launches = rows > 0 ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_transpose_down(const void* w2, int64_t n, int H, int I, void* w2t, void* stream) {
+    g_last_launches = 0;
+    if (!w2 || !w2t) return MOE_EINVAL;
+    if (n < 0 || H <= 0 || I <= 0) return MOE_ESHAPE;
+    if (moe::launch_transpose_bf16(static_cast<const uint16_t*>(w2), n, H, I, static_cast<uint16_t*>(w2t),
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ECUDA;
+    }
+    g_last_launches = n > 0 ? 1 : 0;
     return MOE_OK;
 }
 

@@ -9,6 +9,8 @@ namespace moe {
 cudaError_t launch_layer_bf16(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
 cudaError_t launch_layer_mxfp4(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
 cudaError_t launch_layer_fp8(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
+cudaError_t launch_layer_splitk(const LayerParams& p, cudaStream_t stream, bool pdl, bool coop);
+cudaError_t launch_transpose_bf16(const uint16_t* src, int64_t n, int R, int C, uint16_t* dst, cudaStream_t stream);
 cudaError_t launch_mxfp4_dequant(const uint8_t* codes, const uint8_t* scales, int64_t rows, int K, float* out,
                                  cudaStream_t stream);
 cudaError_t launch_lm_head(const LmParams& p, int wt, cudaStream_t stream, bool pdl);

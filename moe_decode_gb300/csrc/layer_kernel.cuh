@@ -146,8 +146,9 @@ struct ChunkGen {
 };
 
 // Optional phase trace: slot i of this CTA's 16-entry record gets the global
-// timer (ns). Slots 0-7 are written by consumer thread 0, 8-15 by the
-// producer lane.
+// timer (ns). Slots 0-7 are written by the consumer warps, 8-14 by the
+// producer lane, 3 and 15 by the one-token top-k (all logits seen; k rounds
+// done).
 __device__ __forceinline__ void trace_mark(const LayerParams& p, int slot) {
     if (p.trace) p.trace[(size_t)blockIdx.x * 16 + slot] = global_timer_ns();
 }
@@ -1101,7 +1102,10 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
                 }
             }
         }
-        if (__all_sync(0xffffffffu, ok)) break;
+        if (__all_sync(0xffffffffu, ok)) {
+            if (publish && lane == 0) trace_mark(p, 3);  // every tag of this call seen
+            break;
+        }
         if (spin == 0) t0 = global_timer_ns();
         if (aborted(plan)) return false;
         if (global_timer_ns() - t0 > p.timeout_ns) {
@@ -1144,7 +1148,8 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
         const uint32_t e = idx_of(j);
         float kv = sc[j];
         if (!by_logit && bias && e < (uint32_t)E) kv += bias[e];
-        key[j] = e < (uint32_t)E ? f32_key(kv) : 0u;
+        // -0 and +0 rank as equal (ties go to the lower index)
+        key[j] = e < (uint32_t)E ? f32_key(kv == 0.f ? 0.f : kv) : 0u;
     }
     uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
@@ -1186,18 +1191,19 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
             ws = __shfl_sync(0xffffffffu, ws, (int)((we & 63u) >> 1));  // from the winning lane
         if (jj == 0) first = ws;
         if (lane == jj) mine = ws;
-        if (PUBNUM && lane == 0) {  // the slot and its unnormalised weight
+        if (PUBNUM && publish && lane == 0) {  // the slot and its unnormalised weight
             plan->slot_e[jj] = (int16_t)we;
             plan->slot_num[jj] = by_logit ? expf(ws - first) : ws;
             st_release_cta(&plan->known, jj + 1);
         }
     }
+    if (publish && lane == 0) trace_mark(p, 15);  // k rounds done
     const float num = lane < k ? (by_logit ? expf(mine - first) : mine) : 0.f;
     float den = num;
 #pragma unroll
     for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (lane < k) sel_w[lane] = num / den * p.routed_scale;
-    if (PUBNUM && lane == 0) plan->wscale = p.routed_scale / den;
+    if (PUBNUM && publish && lane == 0) plan->wscale = p.routed_scale / den;
     return true;
 }
 

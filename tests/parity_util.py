@@ -96,10 +96,22 @@ def oracle_layer(shape, layer: dict, x_u16: np.ndarray, wfmt: int, idx_override=
 
 
 def expert_weights_of(layer: dict, wfmt: int):
+    """The layer's weights for the C ABI; a layer dict holding w2t (and ws2t)
+    passes the transposed down projections too (split-K one-token layer)."""
     from moe_decode_gb300 import api
     return api.ExpertWeights(w1=layer["w1"], w3=layer["w3"], w2=layer["w2"], ws1=layer["ws1"],
                              ws3=layer["ws3"], ws2=layer["ws2"], s1=layer.get("s1"), s3=layer.get("s3"),
-                             s2=layer.get("s2"))
+                             s2=layer.get("s2"), w2t=layer.get("w2t"), ws2t=layer.get("ws2t"))
+
+
+def with_down_t(layer: dict) -> dict:
+    """A copy of a bf16 layer dict with the transposed down projections
+    (made by the library's moe_transpose_down)."""
+    from moe_decode_gb300 import api
+    d = dict(layer)
+    d["w2t"] = api.transpose_down(layer["w2"])
+    d["ws2t"] = api.transpose_down(layer["ws2"]) if layer["ws2"].numel() else None
+    return d
 
 
 def api_shape(shape, wfmt: int, router=None, io=None):

@@ -41,9 +41,12 @@ def test_library_exports_every_declared_symbol(api):
 def test_workspace_bytes_and_shape_checks(api):
     ling = api.make_shape(2560, 512, 8, 768, 768, 0)
     n1 = api.workspace_bytes(ling, 1)
+    n2 = api.workspace_bytes(ling, 2)
     n16 = api.workspace_bytes(ling, 16)
-    assert 0 < n1 < n16
+    assert 0 < n2 < n16
     assert n16 >= 1024 + 16 * 512 * 4 + 16 * 768 * 2 + 16 * 8 * 768 * 2
+    # one token: room for the split-K layer's partial outputs (MOE_MAX_GRID x H fp32)
+    assert n1 >= 256 * 2560 * 4
     assert api.workspace_bytes(ling, 0) == 0
     assert api.workspace_bytes(ling, 17) == 0
     for bad in (api.make_shape(2500, 512, 8, 768, 768),   # H not a multiple of 256
