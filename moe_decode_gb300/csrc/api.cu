@@ -179,7 +179,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     // one-token MXFP4 layers keep two copies of the tokens: f16 for the
     // routed experts, bf16 for the router and the shared expert
     const bool two = s->wfmt == 1 && M == 1 && mode == moe::kModeLayer;
-    const size_t x_one = align_up((size_t)M * p.H * 2, 128);
+    p.xp = s->wfmt == 0 ? p.H + 8 : p.H;
+    const size_t x_one = align_up((size_t)M * p.xp * 2, 128);
     const size_t x_bytes = x_one * (two ? 2 : 1);
     // down-projection results per (pair, output row): [M + M*k][rpc]; the
     // split-K layer keeps its cross-warp sums there instead

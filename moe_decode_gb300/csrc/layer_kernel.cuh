@@ -66,13 +66,18 @@ __device__ __forceinline__ int swz_vec(int v, int xm) { return v ^ ((v >> 3) & x
 // the routed gate/up rows (phase 2) are claimed dynamically instead
 // (issue_routed_gateup). next() returns false at the end of each phase;
 // begin(ph) starts a phase.
-template <int WFMT>
+// PAD (the general bf16 kernel): a gate/up chunk for the tensor cores holds
+// at most four row pairs, and each weight row sits in its stage at a pitch of
+// its bytes + 16, so that the eight rows an ldmatrix reads fall into eight
+// different 16-byte bank groups.
+template <int WFMT, bool PAD = false>
 __device__ __forceinline__ int gateup_cap(const LayerParams& p, bool routed) {
     // a routed row pair: codes plus scales (MXFP4 and FP8 both carry H / 32
     // scale bytes per row)
-    uint32_t pair = !routed || WFMT == 0 ? (uint32_t)(4 * p.H)
+    uint32_t pair = !routed || WFMT == 0 ? (uint32_t)(4 * p.H + (PAD ? 32 : 0))
                     : (uint32_t)(2 * ((WFMT == 1 ? p.H / 2 : p.H) + p.H / 32));
-    return (int)(SB / pair);
+    // a tensor-core chunk is one 8-column tile: at most four row pairs
+    return PAD ? min(4, (int)(SB / pair)) : (int)(SB / pair);
 }
 
 template <int WFMT>
@@ -81,7 +86,11 @@ __device__ __forceinline__ uint32_t down_rowbytes(const LayerParams& p, int slot
     return WFMT == 0 ? (uint32_t)p.I * 2 : (uint32_t)((WFMT == 1 ? p.I / 2 : p.I) + p.I / 32);
 }
 
-template <int WFMT>
+// Tensor-core gate/up (the general bf16 kernel) for slots with at least this
+// many tokens; below it the CUDA-core dots cost fewer instructions.
+constexpr int kMmaMinTokens = 6;
+
+template <int WFMT, bool PAD = false>
 struct ChunkGen {
     int phase;
     int a, b, cap;                 // phases 0, 1: row cursor, end, rows per chunk
@@ -97,7 +106,7 @@ struct ChunkGen {
         } else if (ph == 1) {
             a = (int)(cc * (uint32_t)p.Is / G);
             b = (int)((cc + 1) * (uint32_t)p.Is / G);
-            cap = gateup_cap<WFMT>(p, false);
+            cap = gateup_cap<WFMT, PAD>(p, false);
         } else {
             nslot = plan->nslot;
             h0 = (int)(cc * (uint32_t)p.H / G);
@@ -225,7 +234,7 @@ struct Ring {
 // is free; the activation tiles of a down chunk are produced by all CTAs and
 // may only be fetched after grid barrier 2, so until then they wait in a
 // short list in shared memory.
-template <int WFMT>
+template <int WFMT, bool PAD = false>
 struct Producer {
     const LayerParams& p;
     Plan* plan;
@@ -304,6 +313,9 @@ struct Producer {
         } else if (ch.kind == 1) {
             if (ch.slot < 0 || WFMT == 0) {
                 const uint32_t b = (uint32_t)ch.n * p.H * 2;
+                const int np = ch.slot < 0 ? p.M : plan->slot_p0[ch.slot + 1] - plan->slot_p0[ch.slot];
+                const bool mma = PAD && np >= kMmaMinTokens;
+                if (mma) plan->desc[ring.s].kind = 5;
                 const uint8_t *a, *c;
                 if (ch.slot < 0) {
                     a = reinterpret_cast<const uint8_t*>(p.ws1 + (size_t)ch.r0 * p.H);
@@ -314,8 +326,16 @@ struct Producer {
                     c = p.w3 + off;
                 }
                 mbar_arrive_expect_tx(bar, 2 * b);
-                bulk_g2s(dst, a, b, bar, pol_w);
-                bulk_g2s(dst + b, c, b, bar, pol_w);
+                if (mma) {  // one copy per row, rows at a padded pitch
+                    const uint32_t rb = (uint32_t)p.H * 2, pitch = rb + 16;
+                    for (int j = 0; j < ch.n; ++j) {
+                        bulk_g2s(dst + (uint32_t)j * pitch, a + (size_t)j * rb, rb, bar, pol_w);
+                        bulk_g2s(dst + (uint32_t)(ch.n + j) * pitch, c + (size_t)j * rb, rb, bar, pol_w);
+                    }
+                } else {
+                    bulk_g2s(dst, a, b, bar, pol_w);
+                    bulk_g2s(dst + b, c, b, bar, pol_w);
+                }
             } else {
                 constexpr int CD = WFMT == 1 ? 2 : 1;  // elements per code byte
                 const uint32_t bc = (uint32_t)ch.n * (p.H / CD), bs = (uint32_t)ch.n * (p.H / 32);
@@ -330,19 +350,22 @@ struct Producer {
             const int inter = ch.slot < 0 ? p.Is : p.I;
             const uint32_t hb = (uint32_t)ch.np * inter * 2;
             const void* hsrc;
-            if (ch.slot < 0) {
-                hsrc = p.hs + (size_t)ch.p0 * p.Is;
-                const uint32_t wb = (uint32_t)ch.n * p.Is * 2;
+            if (ch.slot < 0 || WFMT == 0) {
+                const uint8_t* w;
+                if (ch.slot < 0) {
+                    hsrc = p.hs + (size_t)ch.p0 * p.Is;
+                    w = reinterpret_cast<const uint8_t*>(p.ws2 + (size_t)ch.r0 * p.Is);
+                } else {
+                    hsrc = p.hr + (size_t)(plan->slot_p0[ch.slot] + ch.p0) * p.I;
+                    w = p.w2 + ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * p.I * 2;
+                }
+                const uint32_t rb = (uint32_t)inter * 2, wb = (uint32_t)ch.n * rb;
                 mbar_arrive_expect_tx(bar, hb + wb);
-                bulk_g2s(dst + hb, p.ws2 + (size_t)ch.r0 * p.Is, wb, bar, pol_w);
+                bulk_g2s(dst + hb, w, wb, bar, pol_w);
             } else {
                 hsrc = p.hr + (size_t)(plan->slot_p0[ch.slot] + ch.p0) * p.I;
                 const size_t row = (size_t)plan->slot_e[ch.slot] * p.H + ch.r0;
-                if (WFMT == 0) {
-                    const uint32_t wb = (uint32_t)ch.n * p.I * 2;
-                    mbar_arrive_expect_tx(bar, hb + wb);
-                    bulk_g2s(dst + hb, p.w2 + row * p.I * 2, wb, bar, pol_w);
-                } else {
+                {
                     constexpr int CD = WFMT == 1 ? 2 : 1;
                     const uint32_t bc = (uint32_t)ch.n * (p.I / CD);
                     const size_t s0 = row * (p.I / 32), s1 = s0 + (size_t)ch.n * (p.I / 32);
@@ -781,7 +804,13 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 // TWO: one-token MXFP4 launches, which hold the tokens twice, in f16 times
 // 2^s_t (swizzled) for the routed experts and in plain bf16 for the router
 // and the shared expert (the bf16 mixed-precision fma).
-template <int WFMT, bool TWO>
+// MMA: the general bf16 kernel, whose gate/up rows of slots with at least
+// kMmaMinTokens tokens run on the tensor cores (mma.sync m16n8k16, bf16 x
+// bf16 -> fp32): the slot's tokens (up to 16) are the 16-row operand, eight
+// weight rows the 8-column one. Token rows (p.xp elements apart: H + 8 for
+// bf16 layers) and those weight rows (in a stage) sit at a pitch of their
+// bytes + 16, so that every ldmatrix is free of bank conflicts.
+template <int WFMT, bool TWO, bool MMA = false>
 struct Consumer {
     static constexpr int NCW = consumer_warps(WFMT);
     const LayerParams& p;
@@ -815,7 +844,7 @@ struct Consumer {
         return reinterpret_cast<const uint4*>(xb + (size_t)tok * p.H);
     }
     __device__ __forceinline__ const uint4* xrow(int tok) const {
-        return reinterpret_cast<const uint4*>(xs + (size_t)tok * p.H);
+        return reinterpret_cast<const uint4*>(xs + (size_t)tok * p.xp);
     }
 
     // Router rows: logits[t][e] = Wg[e] . x_t, one warp per row.
@@ -871,9 +900,59 @@ struct Consumer {
         }
     }
 
+    // Gate/up on the tensor cores (chunks of kind 5): one warp per chunk (up
+    // to four row pairs: column 2j of the 8-column operand is gate row j,
+    // column 2j + 1 up row j), all tokens of the slot in one 16-row operand,
+    // K = H in steps of 16 with two accumulators. Each lane then holds g and u
+    // of one row pair for two tokens and stores h = silu(g) * u in bf16.
+    __device__ __forceinline__ void gateup_mma(const Chunk& ch, const uint8_t* st) {
+        if (claim_rows(1) != 0) return;
+        const bool shared = ch.slot < 0;
+        const int inter = shared ? p.Is : p.I;
+        const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
+        const int npairs = shared ? p.M : plan->slot_p0[ch.slot + 1] - pbase;
+        const int n = ch.n;
+        const uint32_t pitch = (uint32_t)p.H * 2 + 16;
+        const int nn = lane & 7, jr = (nn >> 1) < n ? nn >> 1 : 0;
+        const uint32_t baddr = smem_u32(st) + (uint32_t)((nn & 1) ? n + jr : jr) * pitch + ((lane >> 3) & 1) * 16u;
+        const int qa = (lane & 7) + ((lane >> 3) & 1) * 8, khalf = lane >> 4;
+        const int tq = qa < npairs ? qa : 0;
+        const int tok = shared ? tq : plan->pair_tok[pbase + tq];
+        const uint32_t arow = smem_u32(xs) + (uint32_t)tok * p.xp * 2 + (uint32_t)khalf * 16u;
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int nks = p.H / 16;
+#pragma unroll 4
+        for (int ks = 0; ks < nks; ks += 2) {
+            uint32_t a[4], b[2], a2[4], b2[2];
+            ldsm_x4(arow + (uint32_t)ks * 32u, a);
+            ldsm_x2(baddr + (uint32_t)ks * 32u, b);
+            ldsm_x4(arow + (uint32_t)ks * 32u + 32u, a2);
+            ldsm_x2(baddr + (uint32_t)ks * 32u + 32u, b2);
+            mma_bf16_16816(d0, a, b);
+            mma_bf16_16816(d1, a2, b2);
+        }
+        const int g = lane >> 2, t = lane & 3;
+        if (t < n) {
+            const int e = ch.r0 + t;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int q = g + 8 * half;
+                if (q < npairs) {
+                    const int pair = pbase + q;
+                    const float gs = d0[2 * half] + d1[2 * half], us = d0[2 * half + 1] + d1[2 * half + 1];
+                    (shared ? p.hs : p.hr)[(size_t)pair * inter + e] = f32_to_bf16_bits(silu_mul(gs, us));
+                }
+            }
+        }
+    }
+
     // Gate/up rows: one warp per row pair, all tokens of the slot; stores
     // h = silu(g) * u in bf16.
     __device__ __forceinline__ void gateup(const Chunk& ch, const uint8_t* st) {
+        if (MMA && ch.kind == 5) {
+            gateup_mma(ch, st);
+            return;
+        }
         const int j0 = claim_rows(ch.n);
         if (j0 >= ch.n) return;
         const bool shared = ch.slot < 0;
@@ -1037,7 +1116,7 @@ struct Consumer {
             const uint8_t* st = stage_ptr();
             if (ch.kind == 0)
                 router(ch, st);
-            else if (ch.kind == 1)
+            else if (ch.kind == 1 || ch.kind == 5)
                 gateup(ch, st);
             else
                 down(ch, st);
@@ -1287,11 +1366,12 @@ static __device__ void build_plan(const LayerParams& p, Plan* plan, int tid, int
 // token is x = bf16(h / rms * g), rms = sqrt(mean(h^2) + eps). MXFP4 layers
 // hold the tokens in f16 times 2^s_t (x_inv[t] = 2^-s_t), s_t chosen from
 // the token's largest magnitude (exact for bf16 values in f16's normal
-// range). Not inlined: it runs once per launch and keeps the kernel's other
-// code compact; its arguments are plain values.
+// range). Token row t starts xpv vectors after row t - 1. Not inlined: it
+// runs once per launch and keeps the kernel's other code compact; its
+// arguments are plain values.
 template <int WFMT, bool TWO>
 __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const uint4* __restrict__ gam, int M, int H,
-                                         float eps, uint4* __restrict__ dst, uint4* __restrict__ dstb,
+                                         int xpv, float eps, uint4* __restrict__ dst, uint4* __restrict__ dstb,
                                          float* __restrict__ x_inv, int warp, int lane, int nwarps) {
     const int nvt = H / 8;
     for (int t = warp; t < M; t += nwarps) {
@@ -1326,7 +1406,7 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
                 v.y = f32_to_bf16_bits(f[2]) | ((uint32_t)f32_to_bf16_bits(f[3]) << 16);
                 v.z = f32_to_bf16_bits(f[4]) | ((uint32_t)f32_to_bf16_bits(f[5]) << 16);
                 v.w = f32_to_bf16_bits(f[6]) | ((uint32_t)f32_to_bf16_bits(f[7]) << 16);
-                dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
+                dst[(size_t)t * xpv + swz_vec(i, kXM<WFMT>)] = v;
             }
             continue;
         }
@@ -1349,7 +1429,7 @@ __device__ __noinline__ void load_tokens(const uint4* __restrict__ src, const ui
             v.y = f32x2_to_f16x2(f[2] * sc, f[3] * sc);
             v.z = f32x2_to_f16x2(f[4] * sc, f[5] * sc);
             v.w = f32x2_to_f16x2(f[6] * sc, f[7] * sc);
-            dst[(size_t)t * nvt + swz_vec(i, kXM<WFMT>)] = v;
+            dst[(size_t)t * xpv + swz_vec(i, kXM<WFMT>)] = v;
             if (TWO) {  // the plain bf16 copy (the values are bf16 already)
                 uint4 b;
                 b.x = f32_to_bf16_bits(f[0]) | ((uint32_t)f32_to_bf16_bits(f[1]) << 16);
@@ -1389,10 +1469,10 @@ __device__ __forceinline__ bool wait_known(const LayerParams& p, Plan* plan, int
     }
 }
 
-template <int WFMT>
-__device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT>& pr, const LayerParams& p, Plan* plan,
+template <int WFMT, bool PAD>
+__device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT, PAD>& pr, const LayerParams& p, Plan* plan,
                                                     bool incremental) {
-    const uint32_t cap = (uint32_t)gateup_cap<WFMT>(p, true), I = (uint32_t)p.I;
+    const uint32_t cap = (uint32_t)gateup_cap<WFMT, PAD>(p, true), I = (uint32_t)p.I;
     const uint32_t cps = (I + cap - 1) / cap;  // chunks per slot
     if (incremental && !wait_known<WFMT>(p, plan, 1)) return false;
     const uint32_t U = (uint32_t)plan->nslot * cps;
@@ -1422,6 +1502,8 @@ template <int WFMT, bool IO, bool ONE>
 __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
     constexpr int NCW = consumer_warps(WFMT);
     constexpr int NCT = NCW * 32;
+    // bf16 experts with more than a one-token plan: the tensor-core path
+    constexpr bool MMA = WFMT == 0 && !ONE;
     extern __shared__ __align__(1024) uint8_t smem[];
     // Early trigger: the next launch on the stream may start its prologue
     // (weight prefetch) as soon as SMs free up; it still waits for this grid
@@ -1453,14 +1535,14 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
     const bool has_route = (p.mode & kModeRoute) != 0, has_ffn = (p.mode & kModeFfn) != 0;
     // One token: the plan is built incrementally, one slot per top-k round
     constexpr bool incremental = ONE;
-    ChunkGen<WFMT> gen;
+    ChunkGen<WFMT, MMA> gen;
     Chunk ch;
 
     if (warp == NCW) {
         // ---------------- producer (one elected lane)
         if (lane == 0) {
             trace_mark(p, 8);
-            Producer<WFMT> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u};
+            Producer<WFMT, MMA> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u};
             bool ok = true;
             // producer-independent tiles: router rows, shared-expert gate/up
             // rows; an end marker closes each phase of the consumers
@@ -1493,8 +1575,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         const int h0 = (int)((uint32_t)cta * (uint32_t)p.H / (uint32_t)p.G);
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
         constexpr bool TWO = ONE && WFMT == 1;
-        Consumer<WFMT, TWO> cs{p, plan, ring0, xs, reinterpret_cast<const uint16_t*>(smem + p.off_xb), ypair,
-                               warp, lane, 0, h0};
+        Consumer<WFMT, TWO, MMA> cs{p, plan, ring0, xs, reinterpret_cast<const uint16_t*>(smem + p.off_xb), ypair,
+                                    warp, lane, 0, h0};
         const float* bias_s = p.bias ? reinterpret_cast<const float*>(smem + p.off_bias) : nullptr;
         // The router's selection bias is a model parameter, not an output of
         // the previous launch: it is staged before the dependency wait.
@@ -1513,8 +1595,14 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             uint4* dst = reinterpret_cast<uint4*>(xs);
             const int nv = p.M * p.H / 8;
             if (IO) {
-                load_tokens<WFMT, TWO>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.eps, dst,
+                load_tokens<WFMT, TWO>(src, reinterpret_cast<const uint4*>(p.gamma), p.M, p.H, p.xp / 8, p.eps, dst,
                                        reinterpret_cast<uint4*>(smem + p.off_xb), plan->x_inv, warp, lane, NCW);
+            } else if (WFMT == 0 && p.xp != p.H) {
+                const int nvt = p.H / 8, xpv = p.xp / 8;
+                for (int i = tid; i < nv; i += NCT) {
+                    const int t = i / nvt;
+                    dst[i + t * (xpv - nvt)] = __ldg(src + i);
+                }
             } else if (WFMT == 0) {
                 for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
             } else if (WFMT == 2) {

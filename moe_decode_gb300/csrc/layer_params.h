@@ -64,6 +64,9 @@ struct LayerParams {
     float routed_scale;    // routing-weight factor (1 for none)
     int scoring;           // 0 softmax, 1 sigmoid
     int M, H, E, k, I, Is;
+    int xp;                // elements from one token row to the next in shared
+                           // memory (bf16 layers: H + 8, so that tensor-core
+                           // loads of eight token rows hit eight bank groups)
     int mode;
     int G;                 // CTAs in the grid
     int ns;                // ring stages
@@ -79,7 +82,9 @@ struct LayerParams {
 };
 
 // A unit of the ring: the tiles one stage holds. kind 0 router rows, 1
-// gate/up rows, 2 down rows, 3 end of a phase (no data).
+// gate/up rows, 2 down rows, 3 end of a phase (no data), 4 a split-K unit
+// (gate, up and transposed down rows), 5 gate/up rows laid out for the
+// tensor cores (rows at a padded pitch).
 struct Chunk {
     int32_t kind;
     int32_t slot;    // -1 shared expert, else routed slot

@@ -209,7 +209,8 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
         }
         if (IO) {
             load_tokens<0, false>(reinterpret_cast<const uint4*>(p.x), reinterpret_cast<const uint4*>(p.gamma), 1,
-                                  p.H, p.eps, reinterpret_cast<uint4*>(xs), nullptr, plan->x_inv, warp, lane, NCW);
+                                  p.H, p.H / 8, p.eps, reinterpret_cast<uint4*>(xs), nullptr, plan->x_inv, warp, lane,
+                                  NCW);
         } else {
             for (int i = tid; i < nvec; i += NCT) reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
         }

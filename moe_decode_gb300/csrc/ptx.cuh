@@ -173,6 +173,31 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// ---------------------------------------------------------------- tensor cores
+// ldmatrix: four (x4) or two (x2) 8 x 8 tiles of 16-bit elements from shared
+// memory; lanes 8i..8i+7 give the row addresses (16 bytes each) of tile i.
+// Thread l receives row l / 4, elements 2 (l % 4) and 2 (l % 4) + 1 of each
+// tile, in register i.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+// d += a . b for a 16 x 16 (row-major) bf16 tile a and a 16 x 8 (column-major)
+// bf16 tile b, fp32 accumulate (mma.sync m16n8k16). Thread l holds d rows
+// l / 4 (d[0], d[1]) and l / 4 + 8 (d[2], d[3]), columns 2 (l % 4) and
+// 2 (l % 4) + 1.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // ---------------------------------------------------------------- MXFP4
 // Eight e2m1 codes (one 32-bit word; element 2j in the low nibble of byte j)
 // to four f16 pairs with the hardware conversion: w[j] holds elements 2j (low
