@@ -59,6 +59,7 @@ WORKLOADS = {
     "ling_e128_m1": dict(M=1, wfmt=0, copies=2, gen="independent", E=128, fixed_copies=True),
     "ling_e128_m1_splitk": dict(M=1, wfmt=0, copies=2, gen="independent", E=128, fixed_copies=True, down_t=True),
     "ling_e128_m10": dict(M=10, wfmt=0, copies=2, gen="overlap", E=128, fixed_copies=True),
+    "ling_e128_m16": dict(M=16, wfmt=0, copies=2, gen="overlap", E=128, fixed_copies=True),
     "mxfp4_e128_m6": dict(M=6, wfmt=1, copies=2, gen="independent", E=128, fixed_copies=True),
     "fp8_e128_m6": dict(M=6, wfmt=2, copies=2, gen="independent", E=128, fixed_copies=True),
 }
