@@ -186,7 +186,8 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     // split-K layer keeps its cross-warp sums there instead
     size_t y_bytes = align_up((size_t)(M + M * s->top_k) * p.rpc * 4, 128);
     if (splitk) y_bytes = std::max(y_bytes, align_up((size_t)(2 * 10 * 4 + 12 * 32) * 4, 128));
-    const size_t bar_bytes = 128;
+    // mbarriers: full and empty per stage, the plan, per-stage partials
+    const size_t bar_bytes = 256;
     // the router's selection bias, staged before the dependency wait
     const size_t bias_bytes = s->router_bias ? align_up((size_t)s->n_experts * 4, 128) : 0;
     size_t fixed = other_plan + x_bytes + y_bytes + bar_bytes + bias_bytes;

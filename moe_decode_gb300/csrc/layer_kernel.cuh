@@ -87,8 +87,12 @@ __device__ __forceinline__ uint32_t down_rowbytes(const LayerParams& p, int slot
 }
 
 // Tensor-core gate/up (the general bf16 kernel) for slots with at least this
-// many tokens; below it the CUDA-core dots cost fewer instructions.
-constexpr int kMmaMinTokens = 6;
+// many tokens; below it the CUDA-core dots are faster.
+constexpr int kMmaMinTokens = 4;
+// Warps that split the K = H of one tensor-core chunk. A part's 512-byte
+// partial goes into its own k-range of the chunk's rows (32 16-byte slots
+// over as many rows as the range needs: any H of the API fits the stage).
+constexpr int kMmaParts = 3;
 
 template <int WFMT, bool PAD = false>
 struct ChunkGen {
@@ -823,6 +827,8 @@ struct Consumer {
     int qm;              // rows go round-robin over the warps, continuing
                          // across chunks: the running row count mod NCW
     int h0;              // first output row of this CTA
+    uint32_t redph;      // tensor-core chunks: parity bit of each stage's
+                         // partial barrier
 
     __device__ __forceinline__ bool wait_full() { return mbar_wait(ring.full(), ring.ph, p, plan); }
     __device__ __forceinline__ void release() {
@@ -900,29 +906,42 @@ struct Consumer {
         }
     }
 
-    // Gate/up on the tensor cores (chunks of kind 5): one warp per chunk (up
-    // to four row pairs: column 2j of the 8-column operand is gate row j,
-    // column 2j + 1 up row j), all tokens of the slot in one 16-row operand,
-    // K = H in steps of 16 with two accumulators. Each lane then holds g and u
-    // of one row pair for two tokens and stores h = silu(g) * u in bf16.
-    __device__ __forceinline__ void gateup_mma(const Chunk& ch, const uint8_t* st) {
-        if (claim_rows(1) != 0) return;
+    // Gate/up on the tensor cores (chunks of kind 5). The chunk's up to four
+    // row pairs are the 8-column operand (column 2j gate row j, column 2j + 1
+    // up row j), all tokens of the slot the 16-row one, and K = H is split
+    // into kMmaParts parts handed to consecutive warps (continuing round-robin
+    // from chunk to chunk); part q takes k-steps [q nks / P, (q + 1) nks / P)
+    // of the nks = H / 16, with two accumulators. Parts 1.. write their 16 x 8
+    // partial into the first two rows of their own k-range of the stage (bytes
+    // no other warp reads) and arrive on the stage's partial barrier; the warp
+    // of part 0 (the owner) waits for them, sums the parts in order, so that
+    // each lane holds g and u of one row pair for two tokens, and stores h =
+    // silu(g) * u in bf16. The owner's release of the stage comes after that
+    // (its arrival completes the stage's empty barrier), so the partials stay
+    // valid until it has read them.
+    __device__ __forceinline__ bool gateup_mma(const Chunk& ch, const uint8_t* st) {
+        constexpr int P = kMmaParts;
+        const int part = claim_rows(P);
+        const uint32_t rbar = ring.bars + (2u * ring.ns + 1u + ring.s) * 8u, rpar = (redph >> ring.s) & 1u;
+        redph ^= 1u << ring.s;
+        if (part >= P) return true;
+        const int nks = p.H / 16;
+        const uint32_t pitch = (uint32_t)p.H * 2 + 16, sbase = smem_u32(st);
+        const int n = ch.n;
         const bool shared = ch.slot < 0;
-        const int inter = shared ? p.Is : p.I;
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
         const int npairs = shared ? p.M : plan->slot_p0[ch.slot + 1] - pbase;
-        const int n = ch.n;
-        const uint32_t pitch = (uint32_t)p.H * 2 + 16;
+        const int s0 = part * nks / P, s1 = (part + 1) * nks / P;
         const int nn = lane & 7, jr = (nn >> 1) < n ? nn >> 1 : 0;
-        const uint32_t baddr = smem_u32(st) + (uint32_t)((nn & 1) ? n + jr : jr) * pitch + ((lane >> 3) & 1) * 16u;
+        const uint32_t baddr = sbase + (uint32_t)((nn & 1) ? n + jr : jr) * pitch + ((lane >> 3) & 1) * 16u;
         const int qa = (lane & 7) + ((lane >> 3) & 1) * 8, khalf = lane >> 4;
         const int tq = qa < npairs ? qa : 0;
         const int tok = shared ? tq : plan->pair_tok[pbase + tq];
         const uint32_t arow = smem_u32(xs) + (uint32_t)tok * p.xp * 2 + (uint32_t)khalf * 16u;
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        const int nks = p.H / 16;
+        int ks = s0;
 #pragma unroll 4
-        for (int ks = 0; ks < nks; ks += 2) {
+        for (; ks + 1 < s1; ks += 2) {
             uint32_t a[4], b[2], a2[4], b2[2];
             ldsm_x4(arow + (uint32_t)ks * 32u, a);
             ldsm_x2(baddr + (uint32_t)ks * 32u, b);
@@ -931,30 +950,54 @@ struct Consumer {
             mma_bf16_16816(d0, a, b);
             mma_bf16_16816(d1, a2, b2);
         }
+        if (ks < s1) {
+            uint32_t a[4], b[2];
+            ldsm_x4(arow + (uint32_t)ks * 32u, a);
+            ldsm_x2(baddr + (uint32_t)ks * 32u, b);
+            mma_bf16_16816(d0, a, b);
+        }
+        float acc[4] = {d0[0] + d1[0], d0[1] + d1[1], d0[2] + d1[2], d0[3] + d1[3]};
+        // a part's 512-byte partial: lane l's 16 bytes in row l / per_row of
+        // the stage, inside the part's own k-range
+        auto slot_addr = [&](int q) {
+            const int q0 = q * nks / P, per_row = ((q + 1) * nks / P - q0) * 2;
+            return sbase + (uint32_t)(lane / per_row) * pitch + (uint32_t)q0 * 32u + (uint32_t)(lane % per_row) * 16u;
+        };
+        if (part > 0) {
+            __syncwarp();  // every lane of this warp has read its k-range
+            *reinterpret_cast<float4*>(__cvta_shared_to_generic(slot_addr(part))) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(rbar);
+            return true;
+        }
+        if (!mbar_wait(rbar, rpar, p, plan)) return false;
+#pragma unroll
+        for (int q = 1; q < P; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(__cvta_shared_to_generic(slot_addr(q)));
+            acc[0] += v.x, acc[1] += v.y, acc[2] += v.z, acc[3] += v.w;
+        }
         const int g = lane >> 2, t = lane & 3;
         if (t < n) {
+            const int inter = shared ? p.Is : p.I;
             const int e = ch.r0 + t;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int q = g + 8 * half;
-                if (q < npairs) {
-                    const int pair = pbase + q;
-                    const float gs = d0[2 * half] + d1[2 * half], us = d0[2 * half + 1] + d1[2 * half + 1];
-                    (shared ? p.hs : p.hr)[(size_t)pair * inter + e] = f32_to_bf16_bits(silu_mul(gs, us));
-                }
+                if (q < npairs)
+                    (shared ? p.hs : p.hr)[(size_t)(pbase + q) * inter + e] =
+                        f32_to_bf16_bits(silu_mul(acc[2 * half], acc[2 * half + 1]));
             }
         }
+        return true;
     }
 
     // Gate/up rows: one warp per row pair, all tokens of the slot; stores
     // h = silu(g) * u in bf16.
-    __device__ __forceinline__ void gateup(const Chunk& ch, const uint8_t* st) {
-        if (MMA && ch.kind == 5) {
-            gateup_mma(ch, st);
-            return;
-        }
+    __device__ __forceinline__ bool gateup(const Chunk& ch, const uint8_t* st) {
+        if (MMA && ch.kind == 5) return gateup_mma(ch, st);
         const int j0 = claim_rows(ch.n);
-        if (j0 >= ch.n) return;
+        if (j0 >= ch.n) return true;
         const bool shared = ch.slot < 0;
         const int inter = shared ? p.Is : p.I;
         const int pbase = shared ? 0 : plan->slot_p0[ch.slot];
@@ -997,6 +1040,7 @@ struct Consumer {
                 }
             }
         }
+        return true;
     }
 
     // Down projection. A down chunk (one slot, a pair group, a block of
@@ -1116,10 +1160,11 @@ struct Consumer {
             const uint8_t* st = stage_ptr();
             if (ch.kind == 0)
                 router(ch, st);
-            else if (ch.kind == 1 || ch.kind == 5)
-                gateup(ch, st);
-            else
+            else if (ch.kind == 1 || ch.kind == 5) {
+                if (!gateup(ch, st)) return false;
+            } else {
                 down(ch, st);
+            }
             release();
         }
     }
@@ -1523,6 +1568,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             mbar_init(bars + (p.ns + i) * 8, NCW);
         }
         mbar_init(plan_bar, 1);
+        if (MMA)  // per-stage barriers of the tensor-core chunks' partials
+            for (int i = 0; i < p.ns; ++i) mbar_init(plan_bar + 8u + i * 8u, kMmaParts - 1);
         plan->abort = 0;
         plan->npend = 0;
         plan->known = 0;
@@ -1576,7 +1623,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         const int h1 = (int)((uint32_t)(cta + 1) * (uint32_t)p.H / (uint32_t)p.G);
         constexpr bool TWO = ONE && WFMT == 1;
         Consumer<WFMT, TWO, MMA> cs{p, plan, ring0, xs, reinterpret_cast<const uint16_t*>(smem + p.off_xb), ypair,
-                                    warp, lane, 0, h0};
+                                    warp, lane, 0, h0, 0u};
         const float* bias_s = p.bias ? reinterpret_cast<const float*>(smem + p.off_bias) : nullptr;
         // The router's selection bias is a model parameter, not an output of
         // the previous launch: it is staged before the dependency wait.
