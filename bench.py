@@ -75,6 +75,8 @@ LM_WORKLOADS = {
     "lmhead_bf16_m1": dict(M=1, wfmt=0, V=157184, H=2560),
     "lmhead_fp8_m1": dict(M=1, wfmt=2, V=157184, H=2560),
     "lmhead_bf16_m6": dict(M=6, wfmt=0, V=157184, H=2560),
+    "lmhead_bf16_m2": dict(M=2, wfmt=0, V=157184, H=2560),
+    "lmhead_bf16_m16": dict(M=16, wfmt=0, V=157184, H=2560),
 }
 
 

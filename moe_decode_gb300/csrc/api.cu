@@ -403,7 +403,9 @@ int moe_lm_head(const void* x, int M, const void* W, const float* w_scale, int V
     p.timeout_ns = (unsigned long long)g_opt.timeout_ns;
     // barriers and the abort flag in the first 128 bytes, per-token scales
     // (FP8 rows) in the next 128
-    const size_t bar_bytes = 256, x_bytes = align_up((size_t)M * H * 2, 128);
+    // token rows: bf16 launches on the tensor cores keep them H + 8 elements apart
+    const size_t xrow = (size_t)H * 2 + (moe::lm_uses_mma(M, H, wfmt) ? 16 : 0);
+    const size_t bar_bytes = 256, x_bytes = align_up((size_t)M * xrow, 128);
     if ((size_t)dev.smem_optin <= bar_bytes + x_bytes) return MOE_ESHAPE;
     int ns = (int)(((size_t)dev.smem_optin - bar_bytes - x_bytes) / moe::kStageBytes);
     if (ns > moe::kMaxStages) ns = moe::kMaxStages;

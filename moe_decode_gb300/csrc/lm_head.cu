@@ -109,7 +109,13 @@ __device__ __forceinline__ void lm_dot(const uint4* __restrict__ row, const uint
     for (int t = 0; t < NT; ++t) acc[t] = (pa[t][0].x + pa[t][0].y) + (pa[t][1].x + pa[t][1].y);
 }
 
-template <int WT>
+// MMA (bf16 rows, M >= kLmMmaMinTokens): each stage's rows (at most eight,
+// copied one per row at a pitch of their bytes + 16, so that ldmatrix reads
+// of eight rows hit eight bank groups) go to one warp, round-robin, which
+// computes them against all tokens on the tensor cores: the tokens (token
+// rows H + 8 elements apart) are the 16-row operand of mma.sync m16n8k16,
+// the rows the 8 columns, K = H with two accumulators.
+template <int WT, bool MMA>
 __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_constant__ LmParams p) {
     constexpr int NCW = kLmConsumerWarps;
     constexpr int NCT = NCW * 32;
@@ -132,7 +138,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
     const int c = (int)blockIdx.x;
     const int v0 = (int)((int64_t)c * p.V / p.G), v1 = (int)((int64_t)(c + 1) * p.V / p.G);
     const uint32_t rowbytes = (uint32_t)p.H * (WT == 0 ? 2u : 1u);
-    const int cap = (int)(LSB / rowbytes);
+    const uint32_t pitch = MMA ? rowbytes + 16u : rowbytes;  // row pitch in a stage
+    const int cap = MMA ? min(8, (int)(LSB / pitch)) : (int)(LSB / rowbytes);
+    const int xpv = MMA ? p.H / 8 + 1 : p.H / 8;  // token row pitch in 16-byte vectors
     const uint32_t base = smem_u32(smem);
 
     if (warp == NCW) {
@@ -147,7 +155,13 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
                 if (!ok) break;
                 const uint32_t b = (uint32_t)nr * rowbytes;
                 mbar_arrive_expect_tx(bars + s * 8, b);
-                bulk_g2s(base + s * LSB, p.W + (size_t)r * rowbytes, b, bars + s * 8, pol);
+                if (MMA) {
+                    for (int j = 0; j < nr; ++j)
+                        bulk_g2s(base + s * LSB + (uint32_t)j * pitch, p.W + (size_t)(r + j) * rowbytes, rowbytes,
+                                 bars + s * 8, pol);
+                } else {
+                    bulk_g2s(base + s * LSB, p.W + (size_t)r * rowbytes, b, bars + s * 8, pol);
+                }
                 if (++s == (uint32_t)p.ns) {
                     s = 0;
                     ph ^= 1u;
@@ -169,8 +183,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
             uint4* dst = reinterpret_cast<uint4*>(xs);
             if (WT == 0) {
-                const int nv = p.M * p.H / 8;
-                for (int i = tid; i < nv; i += NCT) dst[i] = __ldg(src + i);
+                const int nv = p.M * p.H / 8, nvt = p.H / 8;
+                for (int i = tid; i < nv; i += NCT) dst[i + (i / nvt) * (xpv - nvt)] = __ldg(src + i);
             } else {
                 // FP8 rows: tokens in f16 times 2^s_t, s_t chosen from the
                 // token's largest magnitude (exact for bf16 values in f16's
@@ -208,6 +222,54 @@ __global__ void __launch_bounds__(kLmThreads, 1) lm_head_kernel(const __grid_con
         for (int r = v0; r < v1; r += cap) {
             const int nr = min(cap, v1 - r);
             if (!lm_wait(bars + s * 8, ph, p, flag)) break;
+            if (MMA) {
+                // the stage goes to one warp (round-robin over the stages)
+                if (warp == qm) {
+                    const uint32_t sb = base + s * LSB;
+                    const uint32_t baddr = sb + (uint32_t)min(lane & 7, nr - 1) * pitch + ((lane >> 3) & 1) * 16u;
+                    const int qa = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const uint32_t arow =
+                        smem_u32(xs) + (uint32_t)(qa < p.M ? qa : 0) * xpv * 16u + (uint32_t)(lane >> 4) * 16u;
+                    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+                    const int nks = p.H / 16;
+                    int ks = 0;
+#pragma unroll 4
+                    for (; ks + 1 < nks; ks += 2) {
+                        uint32_t a[4], b[2], a2[4], b2[2];
+                        ldsm_x4(arow + (uint32_t)ks * 32u, a);
+                        ldsm_x2(baddr + (uint32_t)ks * 32u, b);
+                        ldsm_x4(arow + (uint32_t)ks * 32u + 32u, a2);
+                        ldsm_x2(baddr + (uint32_t)ks * 32u + 32u, b2);
+                        mma_bf16_16816(d0, a, b);
+                        mma_bf16_16816(d1, a2, b2);
+                    }
+                    if (ks < nks) {
+                        uint32_t a[4], b[2];
+                        ldsm_x4(arow + (uint32_t)ks * 32u, a);
+                        ldsm_x2(baddr + (uint32_t)ks * 32u, b);
+                        mma_bf16_16816(d0, a, b);
+                    }
+                    // lane (g, t): tokens g and g + 8, rows 2t and 2t + 1
+                    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int q = g + 8 * half;
+                        if (q >= p.M) continue;
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc)
+                            if (2 * t + cc < nr)
+                                p.logits[(size_t)q * p.V + r + 2 * t + cc] = d0[2 * half + cc] + d1[2 * half + cc];
+                    }
+                }
+                qm = qm + 1 == NCW ? 0 : qm + 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars + (p.ns + s) * 8);
+                if (++s == (uint32_t)p.ns) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                continue;
+            }
             const uint8_t* st = reinterpret_cast<const uint8_t*>(__cvta_shared_to_generic(base + s * LSB));
             const int j0 = warp >= qm ? warp - qm : warp - qm + NCW;  // first row of this warp
             qm = (qm + nr) % NCW;
@@ -292,7 +354,9 @@ __global__ void fp8_dequant_kernel(const uint8_t* __restrict__ codes, const floa
 }  // namespace
 
 cudaError_t launch_lm_head(const LmParams& p, int wt, cudaStream_t stream, bool pdl) {
-    void (*kern)(LmParams) = wt == 0 ? lm_head_kernel<0> : lm_head_kernel<2>;
+    void (*kern)(LmParams) = wt != 0                  ? lm_head_kernel<2, false>
+                             : lm_uses_mma(p.M, p.H, wt) ? lm_head_kernel<0, true>
+                                                         : lm_head_kernel<0, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

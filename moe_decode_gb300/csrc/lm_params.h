@@ -7,6 +7,10 @@ namespace moe {
 
 constexpr int kLmConsumerWarps = 11;
 constexpr int kLmThreads = (kLmConsumerWarps + 1) * 32;
+// bf16 rows against at least this many tokens run on the tensor cores (K in
+// steps of 16: H a multiple of 16)
+constexpr int kLmMmaMinTokens = 3;
+inline bool lm_uses_mma(int M, int H, int wt) { return wt == 0 && M >= kLmMmaMinTokens && H % 16 == 0; }
 
 struct LmParams {
     const uint16_t* x;     // [M, H] bf16

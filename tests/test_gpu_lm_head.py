@@ -75,9 +75,10 @@ def _run_lm(api, x, W, V, H, wfmt, scale=None):
     return logits.cpu().numpy()
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 6, 9, 16])
 @pytest.mark.parametrize("wfmt", [0, 2])
 def test_lm_head_small_ragged(api, M, wfmt):
+    """bf16 rows against three or more tokens run on the tensor cores."""
     V, H = 1000, 256                           # 1000 rows over 152 CTAs: uneven
     Wb = synth.normal_bf16(31, 1, 0, V * H, 0.02, "cuda").view(V, H)
     x = synth.normal_bf16(32 + M, 2, 0, M * H, 1.0, "cuda").view(M, H)
@@ -123,6 +124,16 @@ def test_lm_head_token_scales(api, wfmt):
         assert rel_l2(got[t], want[t]) <= TOL, t
 
 
+@pytest.mark.parametrize("M", [2, 5])
+def test_lm_head_h_not_a_multiple_of_16(api, M):
+    """H = 264 (a multiple of 8, not of 16): the CUDA-core path at any M."""
+    V, H = 333, 264
+    Wb = synth.normal_bf16(71, 1, 0, V * H, 0.02, "cuda").view(V, H)
+    x = synth.normal_bf16(72 + M, 2, 0, M * H, 1.0, "cuda").view(M, H)
+    got = _run_lm(api, x, Wb, V, H, 0)
+    assert rel_l2(got, oracle.lm_head(synth.to_u16(x), synth.to_u16(Wb), V)) <= TOL
+
+
 def test_lm_head_fewer_rows_than_ctas(api):
     V, H, M = 7, 512, 5
     Wb = synth.normal_bf16(41, 1, 0, V * H, 0.02, "cuda").view(V, H)
@@ -131,9 +142,9 @@ def test_lm_head_fewer_rows_than_ctas(api):
     assert rel_l2(got, oracle.lm_head(synth.to_u16(x), synth.to_u16(Wb), V)) <= TOL
 
 
-@pytest.mark.parametrize("wfmt", [0, 2])
-def test_lm_head_full_vocabulary_sampled_rows(api, wfmt):
-    V, H, M = 157184, 2560, 2
+@pytest.mark.parametrize("wfmt,M", [(0, 2), (2, 2), (0, 6)])
+def test_lm_head_full_vocabulary_sampled_rows(api, wfmt, M):
+    V, H = 157184, 2560
     Wb = synth.normal_bf16(51, 1, 0, V * H, 0.02, "cuda").view(V, H)
     x = synth.normal_bf16(52, 2, 0, M * H, 1.0, "cuda").view(M, H)
     rows = np.unique(np.concatenate([np.arange(8), np.arange(V - 8, V),
