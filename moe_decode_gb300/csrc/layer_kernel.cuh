@@ -212,6 +212,28 @@ __device__ __forceinline__ bool grid_wait(const unsigned* ctr, unsigned target, 
     return true;
 }
 
+// ------------------------------------------------------------ call counters
+// Grid barrier 2 and the routed gate/up work counter of the call with this
+// epoch (two sets, by parity).
+__device__ __forceinline__ unsigned* ctl_bar2(const LayerParams& p, uint32_t epoch) {
+    return p.ctrl + ((epoch & 1u) ? kCtlBar2Odd : kCtlBar2);
+}
+__device__ __forceinline__ unsigned* ctl_work(const LayerParams& p, uint32_t epoch) {
+    return p.ctrl + ((epoch & 1u) ? kCtlWorkOdd : kCtlWork);
+}
+
+// Called by one CTA once every CTA of the call has read the epoch (all have
+// arrived at a grid barrier after reading it): zeroes the counter set of the
+// next epoch (last used two calls ago, which has finished) and advances the
+// epoch. The next call on the stream reads them only after this grid has
+// finished.
+__device__ __forceinline__ void advance_epoch(const LayerParams& p, uint32_t epoch) {
+    const uint32_t n = epoch + 1u;
+    atomicExch(ctl_bar2(p, n), 0u);
+    atomicExch(ctl_work(p, n), 0u);
+    atomicExch(p.ctrl + kCtlEpoch, n);
+}
+
 // ------------------------------------------------------------ ring
 // Stage cursor of the shared-memory ring, advanced chunk by chunk (no
 // divisions). Chunk n lives in stage n % ns and is the (n / ns)-th use of it;
@@ -247,6 +269,7 @@ struct Producer {
     uint64_t pol_h;  // activations: keep
     bool b2_done;
     uint32_t complete_upto;  // chunks whose copies were all issued
+    uint32_t epoch;          // this call's epoch (read after the dependency wait)
 
     __device__ __forceinline__ void flush_pending() {
         for (int i = 0; i < plan->npend; ++i)
@@ -257,10 +280,11 @@ struct Producer {
 
     __device__ __forceinline__ bool poll_b2(bool block) {
         if (b2_done) return true;
-        const unsigned* ctr = p.ctrl + kCtlBar2;
+        const unsigned* ctr = ctl_bar2(p, epoch);
         const bool ok = block ? grid_wait(ctr, (unsigned)p.G, p, plan) : (ld_acquire_gpu(ctr) >= (unsigned)p.G);
         if (!ok) return false;
         b2_done = true;
+        if (blockIdx.x == 0) advance_epoch(p, epoch);
         fence_proxy_async_global();
         flush_pending();
         return true;
@@ -1521,7 +1545,7 @@ __device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT, PAD>& pr, con
     const uint32_t cps = (I + cap - 1) / cap;  // chunks per slot
     if (incremental && !wait_known<WFMT>(p, plan, 1)) return false;
     const uint32_t U = (uint32_t)plan->nslot * cps;
-    unsigned* wc = p.ctrl + kCtlWork;
+    unsigned* wc = ctl_work(p, pr.epoch);
     uint32_t a = atomicAdd(wc, 1u), b = atomicAdd(wc, 1u);
     bool ok = true;
     while (ok && a < U) {
@@ -1589,7 +1613,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         // ---------------- producer (one elected lane)
         if (lane == 0) {
             trace_mark(p, 8);
-            Producer<WFMT, MMA> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u};
+            Producer<WFMT, MMA> pr{p, plan, ring0, policy_evict_first(), policy_evict_last(), false, 0u, 0u};
             bool ok = true;
             // producer-independent tiles: router rows, shared-expert gate/up
             // rows; an end marker closes each phase of the consumers
@@ -1601,6 +1625,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                 for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
             trace_mark(p, 9);
             pdl_wait();
+            pr.epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
             if (ok && has_ffn) {
                 if (!incremental) ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
@@ -1631,7 +1656,8 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             for (int i = tid; i < p.E; i += NCT) const_cast<float*>(bias_s)[i] = __ldg(p.bias + i);
         pdl_wait();
         if (tid == 0) {
-            plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
+            plan->epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
+            plan->tag = plan->epoch % 0xffffffffu + 1u;
             // a call that ran out of time left the control words stale: every
             // later call on this workspace refuses to run until it is zeroed
             if ((int)ld_acquire_gpu(p.ctrl + kCtlStatus) == -101 /* MOE_ETIMEOUT */)
@@ -1765,7 +1791,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             if (tid == 0) trace_mark(p, 6);
             if (tid == 0 && !aborted(plan)) {
                 __threadfence();
-                atomicAdd(p.ctrl + kCtlBar2, 1u);
+                atomicAdd(ctl_bar2(p, plan->epoch), 1u);
             }
             if (ok) ok = cs.consume_phase();  // down
             named_bar_sync(1, NCT);
@@ -1794,16 +1820,17 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             }
         }
     }
-    __syncthreads();
-    if (tid == 0 && !aborted(plan)) {
-        // Last CTA out re-arms the barrier counters for the next call.
-        __threadfence();
-        const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
-        if (old == (unsigned)p.G - 1u) {
-            atomicExch(p.ctrl + kCtlBar2, 0u);
-            atomicExch(p.ctrl + kCtlWork, 0u);
-            atomicAdd(p.ctrl + kCtlEpoch, 1u);  // the next call's tag
-            atomicExch(p.ctrl + kCtlExit, 0u);
+    if (!has_ffn) {
+        // A routing-only call has no grid barrier: the last CTA out advances
+        // the epoch (the next call's logit tag).
+        __syncthreads();
+        if (tid == 0 && !aborted(plan)) {
+            __threadfence();
+            const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
+            if (old == (unsigned)p.G - 1u) {
+                atomicExch(p.ctrl + kCtlExit, 0u);
+                advance_epoch(p, plan->epoch);
+            }
         }
     }
 }

@@ -19,13 +19,19 @@ constexpr int kMaxEntries = kMaxM * kMaxK;
 constexpr int kMaxGrid = 256;  // CTAs of a split-K layer launch (workspace sizing)
 
 // workspace control block (uint32 words, 128 bytes apart): status, launch
-// epoch (advanced by the last CTA of every call), grid barrier, exit counter,
-// work counter
+// epoch, then grid barrier 2 and the routed gate/up work counter of the calls
+// with an even epoch, the exit counter of routing-only calls, and the barrier
+// and work counter of the calls with an odd epoch. A call with an FFN uses the
+// set of its epoch's parity; once every CTA has passed its grid barrier 2, one
+// CTA zeroes the other set and advances the epoch, so that the next call on
+// the workspace finds its counters at zero and no CTA does any atomics at exit.
 constexpr int kCtlStatus = 0;
 constexpr int kCtlEpoch = 32;
 constexpr int kCtlBar2 = 64;
 constexpr int kCtlExit = 96;
 constexpr int kCtlWork = 128;  // next routed gate/up chunk to claim
+constexpr int kCtlBar2Odd = 160;
+constexpr int kCtlWorkOdd = 192;
 constexpr uint32_t kCtlBytes = 1024;
 
 enum : int { kModeRoute = 1, kModeFfn = 2, kModeLayer = 3 };
@@ -118,7 +124,7 @@ struct Plan {
     int32_t npairs;
     uint32_t tag;                   // this call's tag: 1 + epoch mod (2^32 - 1)
     int32_t abort;
-    int32_t pad;
+    uint32_t epoch;                 // this call's launch epoch
     // Activation copies of down chunks issued before grid barrier 2
     // (producer only): destination, barrier, bytes, source.
     uint32_t pend_dst[kMaxStages], pend_bar[kMaxStages], pend_bytes[kMaxStages];

@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
             for (int i = tid; i < p.E; i += NCT) const_cast<float*>(bias_s)[i] = __ldg(p.bias + i);
         pdl_wait();
         if (tid == 0) {
-            plan->tag = ld_acquire_gpu(p.ctrl + kCtlEpoch) % 0xffffffffu + 1u;
+            plan->epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
+            plan->tag = plan->epoch % 0xffffffffu + 1u;
             if ((int)ld_acquire_gpu(p.ctrl + kCtlStatus) == -101 /* MOE_ETIMEOUT */) set_abort(p, plan, -101);
         }
         if (IO) {
@@ -386,8 +387,9 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
         if (tid == 0) trace_mark(p, 5);
         if (tid == 0 && !aborted(plan)) {
             __threadfence();
-            atomicAdd(p.ctrl + kCtlBar2, 1u);
-            grid_wait(p.ctrl + kCtlBar2, (unsigned)p.G, p, plan);
+            atomicAdd(ctl_bar2(p, plan->epoch), 1u);
+            if (grid_wait(ctl_bar2(p, plan->epoch), (unsigned)p.G, p, plan) && cta == 0)
+                advance_epoch(p, plan->epoch);
         }
         named_bar_sync(1, NCT);
         {
@@ -434,18 +436,6 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
             }
         }
         if (tid == 0) trace_mark(p, 7);
-    }
-    __syncthreads();
-    if (tid == 0 && !aborted(plan)) {
-        // last CTA out re-arms the counters for the next call
-        __threadfence();
-        const unsigned old = atomicAdd(p.ctrl + kCtlExit, 1u);
-        if (old == (unsigned)p.G - 1u) {
-            atomicExch(p.ctrl + kCtlBar2, 0u);
-            atomicExch(p.ctrl + kCtlWork, 0u);
-            atomicAdd(p.ctrl + kCtlEpoch, 1u);
-            atomicExch(p.ctrl + kCtlExit, 0u);
-        }
     }
 }
 

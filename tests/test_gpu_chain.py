@@ -109,3 +109,58 @@ def test_ling_chain_of_four_layers(api, wfmt):
     _run_and_check(api, shapes, layers, wfmt, x0)
     del layers
     torch.cuda.empty_cache()
+
+
+def test_mixed_calls_on_one_workspace(api):
+    """Routing-only, FFN-only, one-token (two-phase and split-K) and
+    multi-token layer calls alternate on one workspace, issued back to back
+    without synchronising. The calls share the workspace's control words: a
+    call with an FFN uses the barrier and work counter of its epoch's parity
+    and advances the epoch once its grid barrier has passed, a routing-only
+    call advances it at exit. Every call is checked against the oracle."""
+    sh = synth.TINY
+    L = pu.with_down_t(synth.device_layer(sh, 21))
+    s = pu.api_shape(sh, 0)
+    k = sh.top_k
+    nbytes = max(api.workspace_bytes(s, m) for m in (1, 6))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    api.workspace_init(ws)
+    W = pu.expert_weights_of(L, 0)
+    W2 = pu.expert_weights_of({n: v for n, v in L.items() if n not in ("w2t", "ws2t")}, 0)
+    plan = ["route", "layer", "ffn", "splitk", "route", "layer", "layer", "route", "splitk", "layer", "ffn", "splitk"]
+    Ms = [3, 1, 5, 1, 1, 6, 1, 2, 1, 2, 4, 1]
+    ffn_idx = {}
+    calls = []
+    for n, (kind, M) in enumerate(zip(plan, Ms)):
+        x = synth.x_independent(sh, 700 + n, M, device="cuda")
+        idx = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+        w = torch.zeros((M, k), dtype=torch.float32, device="cuda")
+        y = torch.zeros((M, sh.hidden), dtype=torch.bfloat16, device="cuda")
+        if kind == "route":
+            api.route(x, L["Wg"], s, idx, w, ws)
+        elif kind == "ffn":
+            rng = np.random.default_rng(800 + n)
+            ih = np.stack([rng.choice(sh.n_experts, k, replace=False) for _ in range(M)]).astype(np.int32)
+            wh = rng.uniform(0.1, 1.0, (M, k)).astype(np.float32)
+            ffn_idx[n] = (ih, wh)
+            idx.copy_(torch.from_numpy(ih))
+            w.copy_(torch.from_numpy(wh))
+            api.ffn(x, idx, w, W2, s, y, ws)
+        else:
+            api.decode_layer(x, L["Wg"], W if kind == "splitk" else W2, s, y, ws, idx, w)
+        calls.append((kind, x, idx, w, y))
+    torch.cuda.synchronize()
+    assert api.read_status(ws) == 0
+    for n, (kind, x, idx, w, y) in enumerate(calls):
+        xu = synth.to_u16(x)
+        if kind == "route":
+            idx_o, w_o, logits_o = oracle.route(xu, synth.to_u16(L["Wg"]), k)
+            pu.check_routing(idx.cpu().numpy(), w.cpu().numpy(), idx_o, w_o, logits_o, k)
+        elif kind == "ffn":
+            ih, wh = ffn_idx[n]
+            _, _, _, y_o = pu.oracle_layer(sh, L, xu, 0, idx_override=ih, w_override=wh)
+            yg = pu.bf16_bits_to_f32(y)
+            assert pu.rel_l2(yg, y_o) <= pu.TOL_Y[0]
+            pu.check_per_token(yg, y_o, pu.TOL_Y[0])
+        else:
+            pu.check_layer_output(sh, L, x, idx.cpu().numpy(), w.cpu().numpy(), y, 0)
