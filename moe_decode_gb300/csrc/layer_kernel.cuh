@@ -1234,19 +1234,26 @@ __device__ __noinline__ bool topk_warp(const unsigned long long* __restrict__ lr
     float lg[EPL];
     uint64_t t0 = 0;
     for (int spin = 0;; ++spin) {
+        // all of a lane's loads are issued before any of their words is
+        // examined, so that one poll costs one round trip, not EPL / 2
+        unsigned long long wa[EPL / 2], wb[EPL / 2];
+#pragma unroll
+        for (int j = 0; j < EPL / 2; ++j) {
+            const int e = 64 * j + 2 * lane;
+            wa[j] = wb[j] = 0ull;
+            if (e < E) ld_relaxed_v2u64(lrow + e, wa[j], wb[j]);
+        }
         bool ok = true;
 #pragma unroll
         for (int j = 0; j < EPL / 2; ++j) {
             const int e = 64 * j + 2 * lane;
             lg[2 * j] = lg[2 * j + 1] = -INFINITY;
             if (e < E) {
-                unsigned long long a, b;
-                ld_relaxed_v2u64(lrow + e, a, b);
-                ok = ok && (uint32_t)(a >> 32) == tag;
-                lg[2 * j] = __uint_as_float((uint32_t)a);
+                ok &= (uint32_t)(wa[j] >> 32) == tag;
+                lg[2 * j] = __uint_as_float((uint32_t)wa[j]);
                 if (e + 1 < E) {
-                    ok = ok && (uint32_t)(b >> 32) == tag;
-                    lg[2 * j + 1] = __uint_as_float((uint32_t)b);
+                    ok &= (uint32_t)(wb[j] >> 32) == tag;
+                    lg[2 * j + 1] = __uint_as_float((uint32_t)wb[j]);
                 }
             }
         }
@@ -1625,7 +1632,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                 for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
             trace_mark(p, 9);
             pdl_wait();
-            pr.epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
+            pr.epoch = ld_relaxed_gpu(p.ctrl + kCtlEpoch);
             if (ok && has_ffn) {
                 if (!incremental) ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
@@ -1655,13 +1662,14 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
         if (p.bias)
             for (int i = tid; i < p.E; i += NCT) const_cast<float*>(bias_s)[i] = __ldg(p.bias + i);
         pdl_wait();
-        if (tid == 0) {
-            plan->epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
-            plan->tag = plan->epoch % 0xffffffffu + 1u;
-            // a call that ran out of time left the control words stale: every
-            // later call on this workspace refuses to run until it is zeroed
-            if ((int)ld_acquire_gpu(p.ctrl + kCtlStatus) == -101 /* MOE_ETIMEOUT */)
-                set_abort(p, plan, -101);
+        // The call's epoch and the status word, read by the last consumer
+        // warp (which loads no token vectors at M = 1), both loads in flight
+        // together and alongside the token loads.
+        const bool ctl_thread = tid == NCT - 32;
+        uint32_t ctl_epoch = 0, ctl_status = 0;
+        if (ctl_thread) {
+            ctl_epoch = ld_relaxed_gpu(p.ctrl + kCtlEpoch);
+            ctl_status = ld_relaxed_gpu(p.ctrl + kCtlStatus);
         }
         {
             const uint4* src = reinterpret_cast<const uint4*>(p.x);
@@ -1724,6 +1732,13 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                     plan->sel_e[i] = p.idx_in[i];
                     plan->sel_w[i] = p.w_in[i];
                 }
+        }
+        if (ctl_thread) {
+            plan->epoch = ctl_epoch;
+            plan->tag = ctl_epoch % 0xffffffffu + 1u;
+            // a call that ran out of time left the control words stale: every
+            // later call on this workspace refuses to run until it is zeroed
+            if ((int)ctl_status == -101 /* MOE_ETIMEOUT */) set_abort(p, plan, -101);
         }
         named_bar_sync(1, NCT);
         if (tid == 0) trace_mark(p, 1);

@@ -203,10 +203,13 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
         if (p.bias)
             for (int i = tid; i < p.E; i += NCT) const_cast<float*>(bias_s)[i] = __ldg(p.bias + i);
         pdl_wait();
-        if (tid == 0) {
-            plan->epoch = ld_acquire_gpu(p.ctrl + kCtlEpoch);
-            plan->tag = plan->epoch % 0xffffffffu + 1u;
-            if ((int)ld_acquire_gpu(p.ctrl + kCtlStatus) == -101 /* MOE_ETIMEOUT */) set_abort(p, plan, -101);
+        // epoch and status: the last consumer warp, both loads in flight
+        // together and alongside the token loads
+        const bool ctl_thread = tid == NCT - 32;
+        uint32_t ctl_epoch = 0, ctl_status = 0;
+        if (ctl_thread) {
+            ctl_epoch = ld_relaxed_gpu(p.ctrl + kCtlEpoch);
+            ctl_status = ld_relaxed_gpu(p.ctrl + kCtlStatus);
         }
         if (IO) {
             load_tokens<0, false>(reinterpret_cast<const uint4*>(p.x), reinterpret_cast<const uint4*>(p.gamma), 1,
@@ -214,6 +217,11 @@ __global__ void __launch_bounds__(block_threads(0), 1) moe_layer_splitk_kernel(c
                                   NCW);
         } else {
             for (int i = tid; i < nvec; i += NCT) reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(p.x) + i);
+        }
+        if (ctl_thread) {
+            plan->epoch = ctl_epoch;
+            plan->tag = ctl_epoch % 0xffffffffu + 1u;
+            if ((int)ctl_status == -101 /* MOE_ETIMEOUT */) set_abort(p, plan, -101);
         }
         named_bar_sync(1, NCT);
         if (tid == 0) trace_mark(p, 1);

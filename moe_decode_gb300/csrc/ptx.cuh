@@ -107,6 +107,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
+// Relaxed GPU-scope 32-bit load: a control word written by an earlier launch
+// that has finished (the dependency wait makes its value visible). Unlike an
+// acquire, it does not hold back the loads that follow it.
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const unsigned* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Release store / acquire load of a 32-bit word at CTA scope (a flag in
 // shared memory that one warp publishes and another polls).
 __device__ __forceinline__ void st_release_cta(int* p, int v) {
