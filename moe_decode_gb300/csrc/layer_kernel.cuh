@@ -1553,14 +1553,26 @@ __device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT, PAD>& pr, con
     if (incremental && !wait_known<WFMT>(p, plan, 1)) return false;
     const uint32_t U = (uint32_t)plan->nslot * cps;
     unsigned* wc = ctl_work(p, pr.epoch);
+    // Each claim takes two consecutive chunks, and the next claim is in
+    // flight while a chunk is issued: half the atomics on the one counter
+    // that every CTA hits (with one chunk per claim the counter's queue held
+    // the stream back: bf16 M = 1 24.4 -> 23.9 us; four per claim leave a
+    // longer tail).
+    constexpr uint32_t kPer = 2;
     uint32_t a = atomicAdd(wc, 1u), b = atomicAdd(wc, 1u);
     bool ok = true;
-    while (ok && a < U) {
-        const uint32_t slot = a / cps, r0 = (a - slot * cps) * cap;
-        if (incremental && !wait_known<WFMT>(p, plan, (int)slot + 1)) return false;
-        const Chunk c{1, (int)slot, (int)r0, (int)min(cap, I - r0), 0, 0};
-        const uint32_t nxt = atomicAdd(wc, 1u);
-        ok = pr.issue(c);
+    while (ok && kPer * a < U) {
+        uint32_t nxt = 0;
+        for (uint32_t h = 0; h < kPer; ++h) {
+            const uint32_t u = kPer * a + h;
+            if (h == 0) nxt = atomicAdd(wc, 1u);
+            if (u >= U) break;
+            const uint32_t slot = u / cps, r0 = (u - slot * cps) * cap;
+            if (incremental && !wait_known<WFMT>(p, plan, (int)slot + 1)) return false;
+            const Chunk c{1, (int)slot, (int)r0, (int)min(cap, I - r0), 0, 0};
+            ok = pr.issue(c);
+            if (!ok) break;
+        }
         a = b;
         b = nxt;
     }
