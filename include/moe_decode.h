@@ -33,11 +33,14 @@
  *    moe_ffn, a bounded wait that ran out) do not fault: they are written to
  *    a status word inside the workspace; read it with moe_read_status.
  *  - A workspace (`ws`, `ws_bytes` >= moe_workspace_bytes(shape, M)) holds
- *    the router logits (each tagged with its call), the SwiGLU activations,
- *    a call counter and the grid-barrier counters. Zero it once with
- *    moe_workspace_init before its first use; every call leaves it ready for
- *    the next. Calls that share a workspace must be ordered on one stream
- *    (or otherwise serialised).
+ *    the router logits (each tagged with its call), the SwiGLU activations
+ *    (for one-token bf16 layers also tagged with the call, with a 16-bit tag
+ *    that repeats every 65,535 calls: calls of several shapes that share a
+ *    workspace should be re-initialised at least that often), a call counter
+ *    and the grid-barrier counters. Zero it once with moe_workspace_init
+ *    before its first use; every call leaves it ready for the next. Calls
+ *    that share a workspace must be ordered on one stream (or otherwise
+ *    serialised).
  *
  * Layouts (row-major; nn.Linear [out, in], contiguous along the reduction
  * dimension):

@@ -111,7 +111,7 @@ int check_shape(const moe_shape* s, int M) {
 }
 
 struct WsLayout {
-    size_t logits, hs, hr, ypart, total;
+    size_t logits, hs, hr, ypart, htag, total;
 };
 
 // splitk: the one-token split-K layer's per-CTA partial outputs follow
@@ -126,6 +126,10 @@ WsLayout ws_layout(const moe_shape* s, int M, bool splitk) {
     off = align_up(off + (size_t)M * s->top_k * s->inter * 2, 256);
     w.ypart = off;
     if (splitk) off = align_up(off + (size_t)MOE_MAX_GRID * s->hidden * 4, 256);
+    // one-token bf16 layers: the tagged activations of the shared expert and
+    // the k routed pairs
+    w.htag = off;
+    if (M == 1 && s->wfmt == 0) off = align_up(off + (size_t)(s->shared_inter + s->top_k * s->inter) * 4, 256);
     w.total = off;
     return w;
 }
@@ -174,6 +178,10 @@ int configure(const moe_shape* s, int M, int mode, void* ws, size_t ws_bytes, La
     p.hs = reinterpret_cast<uint16_t*>(base + wl.hs);
     p.hr = reinterpret_cast<uint16_t*>(base + wl.hr);
     p.ypart = splitk ? reinterpret_cast<float*>(base + wl.ypart) : nullptr;
+    // one-token bf16 layers (not split-K): tagged activations, no barrier 2
+    p.htag = (M == 1 && mode == moe::kModeLayer && s->wfmt == 0 && !splitk)
+                 ? reinterpret_cast<uint32_t*>(base + wl.htag)
+                 : nullptr;
 
     const size_t other_plan = align_up(sizeof(moe::Plan), 128);
     // one-token MXFP4 layers keep two copies of the tokens: f16 for the

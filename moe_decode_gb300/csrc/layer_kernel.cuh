@@ -140,12 +140,13 @@ struct ChunkGen {
             if (q0 >= npairs) {
                 if (++ds >= nslot) return false;
                 npairs = ds < 0 ? p.M : plan->slot_p0[ds + 1] - plan->slot_p0[ds];
-                const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * 2;
+                const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * (!PAD && p.htag ? 4 : 2);
                 pg = max(1, min(npairs, (int)((SB / 2) / hrow)));
                 q0 = 0;
             }
-            // chunk geometry of this (slot, pair group), computed once
-            const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * 2;
+            // chunk geometry of this (slot, pair group), computed once; tagged
+            // activations take four bytes a value
+            const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * (!PAD && p.htag ? 4 : 2);
             const uint32_t reserve = (WFMT != 0 && ds >= 0) ? 32u : 0u;
             np = min(pg, npairs - q0);
             rcap = (int)((SB - (uint32_t)np * hrow - reserve) / down_rowbytes<WFMT>(p, ds));
@@ -221,18 +222,26 @@ __device__ __forceinline__ unsigned* ctl_bar2(const LayerParams& p, uint32_t epo
 __device__ __forceinline__ unsigned* ctl_work(const LayerParams& p, uint32_t epoch) {
     return p.ctrl + ((epoch & 1u) ? kCtlWorkOdd : kCtlWork);
 }
+__device__ __forceinline__ unsigned* ctl_entry(const LayerParams& p, uint32_t epoch) {
+    return p.ctrl + ((epoch & 1u) ? kCtlEntryOdd : kCtlEntry);
+}
 
 // Called by one CTA once every CTA of the call has read the epoch (all have
-// arrived at a grid barrier after reading it): zeroes the counter set of the
-// next epoch (last used two calls ago, which has finished) and advances the
-// epoch. The next call on the stream reads them only after this grid has
-// finished.
+// arrived at a grid barrier, or counted themselves in, after reading it):
+// zeroes the counter set of the next epoch (last used two calls ago, which
+// has finished) and advances the epoch. The next call on the stream reads
+// them only after this grid has finished.
 __device__ __forceinline__ void advance_epoch(const LayerParams& p, uint32_t epoch) {
     const uint32_t n = epoch + 1u;
     atomicExch(ctl_bar2(p, n), 0u);
     atomicExch(ctl_work(p, n), 0u);
+    atomicExch(ctl_entry(p, n), 0u);
     atomicExch(p.ctrl + kCtlEpoch, n);
 }
+
+// The 16-bit tag of a one-token call's activation words: 1 + epoch mod 65535
+// (never 0, and never the previous call's).
+__device__ __forceinline__ uint32_t htag16(const Plan* plan) { return plan->epoch % 0xffffu + 1u; }
 
 // ------------------------------------------------------------ ring
 // Stage cursor of the shared-memory ring, advanced chunk by chunk (no
@@ -330,7 +339,9 @@ struct Producer {
 
     __device__ __forceinline__ bool issue(const Chunk& ch) {
         if (aborted(plan)) return false;
-        if (!acquire(ch.kind == 2)) return false;
+        // down chunks poll barrier 2 while they wait for a stage, unless the
+        // activations come tagged (no barrier 2)
+        if (!acquire(ch.kind == 2 && (PAD || !p.htag))) return false;
         plan->desc[ring.s] = ch;
         const uint32_t dst = ring.stage(), bar = ring.full();
         bool deferred = false;
@@ -374,6 +385,17 @@ struct Producer {
                 bulk_g2s(dst + 2 * bc, p.s1 + row * (p.H / 32), bs, bar, pol_w);
                 bulk_g2s(dst + 2 * bc + bs, p.s3 + row * (p.H / 32), bs, bar, pol_w);
             }
+        } else if (WFMT == 0 && !PAD && p.htag) {
+            // one token: the pair's tagged activations come with the weights
+            const int inter = ch.slot < 0 ? p.Is : p.I;
+            const uint32_t hb = (uint32_t)ch.np * inter * 4, rb = (uint32_t)inter * 2, wb = (uint32_t)ch.n * rb;
+            const uint32_t* hsrc = p.htag + (ch.slot < 0 ? (size_t)ch.p0 * p.Is
+                                                          : (size_t)p.Is + (size_t)(plan->slot_p0[ch.slot] + ch.p0) * p.I);
+            const uint8_t* w = ch.slot < 0 ? reinterpret_cast<const uint8_t*>(p.ws2 + (size_t)ch.r0 * p.Is)
+                                           : p.w2 + ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * p.I * 2;
+            mbar_arrive_expect_tx(bar, hb + wb);
+            bulk_g2s(dst, hsrc, hb, bar, pol_h);
+            bulk_g2s(dst + hb, w, wb, bar, pol_w);
         } else {
             const int inter = ch.slot < 0 ? p.Is : p.I;
             const uint32_t hb = (uint32_t)ch.np * inter * 2;
@@ -622,6 +644,40 @@ __device__ __forceinline__ void dot4_bf16(const uint4* __restrict__ row0, int rs
     for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[j][t] = pa[j][t].x + pa[j][t].y;
+}
+
+// One token, tagged activations: dot4_bf16<1> with the activations held as
+// 32-bit words, a 16-bit tag in the high half and the bf16 value in the low
+// half (two 16-byte words per eight values). Returns false when any word
+// this lane read carries another tag.
+__device__ __forceinline__ bool dot4_bf16_tagged(const uint4* __restrict__ row0, int rstride, int nrow,
+                                                 const uint4* __restrict__ ht, int nvec, int lane, uint32_t tag,
+                                                 float (&acc)[4][1]) {
+    const uint4* rows[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rows[j] = row0 + min(j, nrow - 1) * rstride;
+    float2 pa[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pa[j] = make_float2(0.f, 0.f);
+    uint32_t bad = 0;
+#pragma unroll 2
+    for (int v = lane; v < nvec; v += 32) {
+        const uint4 a = ht[2 * v], b = ht[2 * v + 1];
+        bad |= ((a.x >> 16) ^ tag) | ((a.y >> 16) ^ tag) | ((a.z >> 16) ^ tag) | ((a.w >> 16) ^ tag) |
+               ((b.x >> 16) ^ tag) | ((b.y >> 16) ^ tag) | ((b.z >> 16) ^ tag) | ((b.w >> 16) ^ tag);
+        const uint32_t hh[4] = {__byte_perm(a.x, a.y, 0x5410), __byte_perm(a.z, a.w, 0x5410),
+                                __byte_perm(b.x, b.y, 0x5410), __byte_perm(b.z, b.w, 0x5410)};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 w = rows[j][v];
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fma_bf16x2(ww[e], hh[e], pa[j].x, pa[j].y);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][0] = pa[j].x + pa[j].y;
+    return bad == 0;
 }
 
 // ---- MXFP4 with f16 block sums. The codes of a 32-element block become
@@ -1060,10 +1116,64 @@ struct Consumer {
                 float us = __shfl_down_sync(0xffffffffu, gs, 16);
                 if (lane == 0) {
                     if (WFMT == 1 && shared && !TWO) gs *= plan->x_inv[ta], us *= plan->x_inv[ta];
-                    hdst[(size_t)q0 * inter + col] = f32_to_bf16_bits(silu_mul(gs, us));
+                    const uint32_t hv = f32_to_bf16_bits(silu_mul(gs, us));
+                    if (WFMT == 0 && !MMA && p.htag)  // one token: the word carries the call's tag
+                        st_relaxed_u32(p.htag + (shared ? 0 : p.Is + (size_t)(pbase + q0) * inter) + col,
+                                       (htag16(plan) << 16) | hv);
+                    else
+                        hdst[(size_t)q0 * inter + col] = (uint16_t)hv;
                 }
             }
         }
+        return true;
+    }
+
+    // One-token bf16 layers: polls (bounded) the tagged activations of a down
+    // chunk's pair where the CTAs store them until every tag is this call's,
+    // all of a lane's loads issued before any is examined, and writes them
+    // over the stage's copy (other warps may do the same: they write the same
+    // words). False when the wait ran out or the CTA aborted.
+    __device__ __noinline__ bool refresh_tagged_h(const Chunk& ch, const uint8_t* st) {
+        const uint32_t tag = htag16(plan);
+        const int inter = ch.slot < 0 ? p.Is : p.I;
+        const uint32_t* src = p.htag + (ch.slot < 0 ? (size_t)ch.p0 * p.Is
+                                                    : (size_t)p.Is + (size_t)(plan->slot_p0[ch.slot] + ch.p0) * p.I);
+        uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(st));
+        const int nv = inter / 4;  // 16-byte vectors
+        for (int v0 = 0; v0 < nv; v0 += 8 * 32) {
+            const uint64_t t0 = global_timer_ns();
+            while (true) {
+                uint4 w[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int v = v0 + lane + 32 * j;
+                    w[j] = make_uint4(tag << 16, tag << 16, tag << 16, tag << 16);
+                    if (v < nv) w[j] = ld_relaxed_v4u32(src + 4 * v);
+                }
+                bool cur = true;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    cur &= (w[j].x >> 16) == tag && (w[j].y >> 16) == tag && (w[j].z >> 16) == tag &&
+                           (w[j].w >> 16) == tag;
+                if (__all_sync(0xffffffffu, cur)) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int v = v0 + lane + 32 * j;
+                        if (v < nv) dst[v] = w[j];
+                    }
+                    break;
+                }
+                const bool stop = aborted(plan) || global_timer_ns() - t0 > p.timeout_ns;
+                if (__any_sync(0xffffffffu, stop)) {
+                    if (lane == 0 && !aborted(plan)) set_abort(p, plan, -101 /* MOE_ETIMEOUT */);
+                    return false;
+                }
+                __nanosleep(64);
+            }
+        }
+        // the stage is next written by a bulk copy
+        fence_proxy_async_shared();
+        __syncwarp();
         return true;
     }
 
@@ -1085,6 +1195,31 @@ struct Consumer {
             sofs = s0 - (s0 & ~(size_t)15);
         }
         const int inter = shared ? p.Is : p.I;
+        if (WFMT == 0 && !MMA && p.htag) {
+            // one token (one pair a chunk), tagged activations in the stage
+            const uint4* ht = reinterpret_cast<const uint4*>(st);
+            const int rstride = inter / 8;
+            const uint32_t tag = htag16(plan);
+            for (int part = part0; part < nparts; part += NCW) {
+                const int r = ch.r0 + 4 * part;
+                const int nrow = min(4, ch.r0 + ch.n - r);
+                const uint4* row0 = reinterpret_cast<const uint4*>(st + (size_t)inter * 4 + (size_t)(r - ch.r0) * inter * 2);
+                float acc[4][1];
+                for (int attempt = 0;; ++attempt) {
+                    const bool cur = dot4_bf16_tagged(row0, rstride, nrow, ht, rstride, lane, tag, acc);
+                    if (__all_sync(0xffffffffu, cur)) break;
+                    // the stage's copy came before every CTA had stored this
+                    // pair: read it again where the CTAs store it
+                    if (attempt > 0) {  // cannot happen: the refreshed words are all current
+                        set_abort(p, plan, -101 /* MOE_ETIMEOUT */);
+                        return;
+                    }
+                    if (!refresh_tagged_h(ch, st)) return;
+                }
+                reduce_store<1>(acc, nrow, ypair + (size_t)gbase * p.rpc + (r - h0));
+            }
+            return;
+        }
         for (int part = part0; part < nparts; part += NCW) {
             const int r = ch.r0 + 4 * part;
             const int nrow = min(4, ch.r0 + ch.n - r);
@@ -1551,6 +1686,9 @@ __device__ __forceinline__ bool issue_routed_gateup(Producer<WFMT, PAD>& pr, con
     const uint32_t cap = (uint32_t)gateup_cap<WFMT, PAD>(p, true), I = (uint32_t)p.I;
     const uint32_t cps = (I + cap - 1) / cap;  // chunks per slot
     if (incremental && !wait_known<WFMT>(p, plan, 1)) return false;
+    // the plan (or the first slot) is published after the consumers stored
+    // the call's epoch
+    pr.epoch = plan->epoch;
     const uint32_t U = (uint32_t)plan->nslot * cps;
     unsigned* wc = ctl_work(p, pr.epoch);
     // Each claim takes two consecutive chunks, and the next claim is in
@@ -1590,6 +1728,8 @@ template <int WFMT, bool IO, bool ONE>
 __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const __grid_constant__ LayerParams p) {
     constexpr int NCW = consumer_warps(WFMT);
     constexpr int NCT = NCW * 32;
+    // one-token bf16 launches: tagged activations instead of grid barrier 2
+    const bool tagged = ONE && WFMT == 0 && p.htag != nullptr;
     // bf16 experts with more than a one-token plan: the tensor-core path
     constexpr bool MMA = WFMT == 0 && !ONE;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1644,7 +1784,6 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                 for (gen.begin(1, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
             trace_mark(p, 9);
             pdl_wait();
-            pr.epoch = ld_relaxed_gpu(p.ctrl + kCtlEpoch);
             if (ok && has_ffn) {
                 if (!incremental) ok = mbar_wait(plan_bar, 0, p, plan);
                 trace_mark(p, 10);
@@ -1655,7 +1794,13 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
                     for (gen.begin(3, p, plan, cta); ok && gen.next(p, plan, ch);) ok = pr.issue(ch);
                 if (ok) ok = pr.issue_end();
                 trace_mark(p, 12);
-                if (ok) ok = pr.poll_b2(true);
+                if (!tagged) {
+                    if (ok) ok = pr.poll_b2(true);
+                } else if (ok && cta == 0) {
+                    // no barrier 2: every CTA counted itself in once it had
+                    // read the epoch (long done by now)
+                    if ((ok = grid_wait(ctl_entry(p, pr.epoch), (unsigned)p.G, p, plan))) advance_epoch(p, pr.epoch);
+                }
                 trace_mark(p, 13);
             }
             if (!ok || aborted(plan)) pr.drain();
@@ -1751,6 +1896,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             // a call that ran out of time left the control words stale: every
             // later call on this workspace refuses to run until it is zeroed
             if ((int)ctl_status == -101 /* MOE_ETIMEOUT */) set_abort(p, plan, -101);
+            if (tagged) red_add_relaxed_gpu(ctl_entry(p, ctl_epoch), 1u);
         }
         named_bar_sync(1, NCT);
         if (tid == 0) trace_mark(p, 1);
@@ -1816,7 +1962,7 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             if (ok) ok = cs.consume_phase();  // shared, then routed gate/up
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
-            if (tid == 0 && !aborted(plan)) {
+            if (tid == 0 && !aborted(plan) && !tagged) {
                 __threadfence();
                 atomicAdd(ctl_bar2(p, plan->epoch), 1u);
             }

@@ -18,13 +18,14 @@ constexpr int kMaxE = 1024;
 constexpr int kMaxEntries = kMaxM * kMaxK;
 constexpr int kMaxGrid = 256;  // CTAs of a split-K layer launch (workspace sizing)
 
-// workspace control block (uint32 words, 128 bytes apart): status, launch
-// epoch, then grid barrier 2 and the routed gate/up work counter of the calls
-// with an even epoch, the exit counter of routing-only calls, and the barrier
-// and work counter of the calls with an odd epoch. A call with an FFN uses the
-// set of its epoch's parity; once every CTA has passed its grid barrier 2, one
-// CTA zeroes the other set and advances the epoch, so that the next call on
-// the workspace finds its counters at zero and no CTA does any atomics at exit.
+// workspace control block (uint32 words, 128 bytes apart but for the two
+// entry counters): status, launch epoch, the exit counter of routing-only
+// calls, and per epoch parity a set of grid barrier 2, routed gate/up work
+// counter and entry counter. A call with an FFN uses the set of its epoch's
+// parity; once every CTA has read the epoch (all have passed grid barrier 2,
+// or all have counted themselves in), one CTA zeroes the other set and
+// advances the epoch, so that the next call on the workspace finds its
+// counters at zero and no CTA does any atomics at exit.
 constexpr int kCtlStatus = 0;
 constexpr int kCtlEpoch = 32;
 constexpr int kCtlBar2 = 64;
@@ -32,6 +33,8 @@ constexpr int kCtlExit = 96;
 constexpr int kCtlWork = 128;  // next routed gate/up chunk to claim
 constexpr int kCtlBar2Odd = 160;
 constexpr int kCtlWorkOdd = 192;
+constexpr int kCtlEntry = 224;     // CTAs that have read the epoch
+constexpr int kCtlEntryOdd = 240;  // (never in use at the same time as 224)
 constexpr uint32_t kCtlBytes = 1024;
 
 enum : int { kModeRoute = 1, kModeFfn = 2, kModeLayer = 3 };
@@ -63,6 +66,13 @@ struct LayerParams {
     int Es;
     uint16_t* hs;          // shared-expert activations [M, Is] bf16
     uint16_t* hr;          // routed activations [M*k, I] bf16, grouped by expert
+    // one-token bf16 layers: the activations of the shared expert and of the
+    // k routed pairs as 32-bit words, a 16-bit tag of the call in the high
+    // half and the bf16 value in the low half, [Is + k*I]; null otherwise.
+    // A down chunk's copy brings its pair's words along with the weights, with
+    // no grid barrier; the consumers check the tags and re-read any pair
+    // whose copy came too early.
+    uint32_t* htag;
     const uint16_t* gamma; // RMSNorm weight [H] bf16, or null (x taken as given)
     float eps;             // RMSNorm epsilon
     int residual;          // 1: y += input

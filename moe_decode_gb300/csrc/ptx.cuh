@@ -116,6 +116,29 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const unsigned* p) {
     return v;
 }
 
+// Relaxed GPU-scope 32-bit store and 4 x 32-bit load (each 32-bit element of
+// the vector is single-copy atomic), and a relaxed reduction (an arrival
+// count that nobody waits on at once).
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4u32(const uint32_t* p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_add_relaxed_gpu(unsigned* p, unsigned v) {
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) writes to the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Release store / acquire load of a 32-bit word at CTA scope (a flag in
 // shared memory that one warp publishes and another polls).
 __device__ __forceinline__ void st_release_cta(int* p, int v) {

@@ -139,6 +139,31 @@ def test_ling_uneven_grid(api, ling):
         api.set_option(api.OPT_GRID_CTAS, 0)
 
 
+def test_ling_one_token_any_grid_bit_equal(api, ling):
+    """One-token bf16 layers hand the activations to the down projection as
+    tagged words copied along with each down chunk, with no grid barrier;
+    a copy made before every CTA had stored its pair is read again. On one
+    CTA the producer copies the first down chunks while the last gate/up rows
+    are still being computed, so that path runs. Every row's dot products and
+    the combine order do not depend on the grid: the output is the same bits
+    on every grid, and matches the oracle."""
+    x = synth.x_independent(synth.LING, 12, 1, device="cuda")
+    ref = None
+    for G in (0, 1, 19, 101):
+        api.set_option(api.OPT_GRID_CTAS, G)
+        try:
+            idx, w, y, st = pu.run_layer(synth.LING, ling, x, 0)
+        finally:
+            api.set_option(api.OPT_GRID_CTAS, 0)
+        assert st == 0, (G, st)
+        if ref is None:
+            ref = (idx, w, y)
+            pu.check_layer_output(synth.LING, ling, x, idx, w, y, 0)
+        else:
+            assert np.array_equal(idx, ref[0]) and np.array_equal(w, ref[1]), G
+            assert torch.equal(y, ref[2]), G
+
+
 def test_ling_deterministic_and_pdl_bit_equal(api, ling):
     x = synth.x_independent(synth.LING, 3, 6, device="cuda")
     _, _, y1, _ = pu.run_layer(synth.LING, ling, x, 0)
