@@ -80,6 +80,16 @@ __device__ __forceinline__ int gateup_cap(const LayerParams& p, bool routed) {
     return PAD ? min(4, (int)(SB / pair)) : (int)(SB / pair);
 }
 
+// Bytes of one slot's segment of a packed MXFP4 / FP8 down chunk (kind 6):
+// the pairs' bf16 activations, n rows of codes, and the rows' scales as
+// copied from a 16-byte aligned window (at most 16 bytes more than they
+// take). Every part is a multiple of 16 bytes.
+template <int WFMT>
+__device__ __forceinline__ uint32_t down_seg_bytes(const LayerParams& p, int npairs, int n) {
+    constexpr int CD = WFMT == 1 ? 2 : 1;
+    return (uint32_t)npairs * p.I * 2 + (uint32_t)n * (p.I / CD) + (((uint32_t)n * (p.I / 32) + 15u) & ~15u) + 16u;
+}
+
 template <int WFMT>
 __device__ __forceinline__ uint32_t down_rowbytes(const LayerParams& p, int slot) {
     if (slot < 0) return (uint32_t)p.Is * 2;
@@ -143,6 +153,30 @@ struct ChunkGen {
                 const uint32_t hrow = (uint32_t)(ds < 0 ? p.Is : p.I) * (!PAD && p.htag ? 4 : 2);
                 pg = max(1, min(npairs, (int)((SB / 2) / hrow)));
                 q0 = 0;
+                if (WFMT != 0 && ds >= 0) {
+                    // MXFP4 / FP8: the CTA's rows of one slot take a fraction
+                    // of a stage; consecutive slots that fit whole share one
+                    const int n = h1 - h0;
+                    uint32_t tot = down_seg_bytes<WFMT>(p, npairs, n);
+                    int k = 1;
+                    if (npairs <= pg && tot <= SB) {
+                        while (k < kMaxPack && ds + k < nslot) {
+                            const int npk = plan->slot_p0[ds + k + 1] - plan->slot_p0[ds + k];
+                            const uint32_t b = down_seg_bytes<WFMT>(p, npk, n);
+                            if ((uint32_t)npk * hrow > SB / 2 || tot + b > SB) break;
+                            tot += b;
+                            ++k;
+                        }
+                    }
+                    if (k > 1) {
+                        ch = Chunk{6, ds, h0, n, 0, k};
+                        ds += k - 1;
+                        npairs = 0;  // the next call starts the slot after these
+                        pg = 1;
+                        h = h1;
+                        return true;
+                    }
+                }
             }
             // chunk geometry of this (slot, pair group), computed once; tagged
             // activations take four bytes a value
@@ -341,7 +375,7 @@ struct Producer {
         if (aborted(plan)) return false;
         // down chunks poll barrier 2 while they wait for a stage, unless the
         // activations come tagged (no barrier 2)
-        if (!acquire(ch.kind == 2 && (PAD || !p.htag))) return false;
+        if (!acquire((ch.kind == 2 || ch.kind == 6) && (PAD || !p.htag))) return false;
         plan->desc[ring.s] = ch;
         const uint32_t dst = ring.stage(), bar = ring.full();
         bool deferred = false;
@@ -396,6 +430,43 @@ struct Producer {
             mbar_arrive_expect_tx(bar, hb + wb);
             bulk_g2s(dst, hsrc, hb, bar, pol_h);
             bulk_g2s(dst + hb, w, wb, bar, pol_w);
+        } else if (WFMT != 0 && ch.kind == 6) {
+            // np routed slots, each segment laid out as a kind-2 chunk; the
+            // activation copies wait for barrier 2 like any other
+            constexpr int CD = WFMT == 1 ? 2 : 1;
+            const uint32_t bc = (uint32_t)ch.n * (p.I / CD);
+            uint32_t tot = 0;
+            for (int k = 0; k < ch.np; ++k) {
+                const int slot = ch.slot + k;
+                const uint32_t hb = (uint32_t)(plan->slot_p0[slot + 1] - plan->slot_p0[slot]) * p.I * 2;
+                const size_t s0 = ((size_t)plan->slot_e[slot] * p.H + ch.r0) * (p.I / 32);
+                const size_t s1 = s0 + (size_t)ch.n * (p.I / 32);
+                tot += hb + bc + (uint32_t)(((s1 + 15) & ~(size_t)15) - (s0 & ~(size_t)15));
+            }
+            mbar_arrive_expect_tx(bar, tot);
+            uint32_t off = 0;
+            for (int k = 0; k < ch.np; ++k) {
+                const int slot = ch.slot + k;
+                const int npairs = plan->slot_p0[slot + 1] - plan->slot_p0[slot];
+                const uint32_t hb = (uint32_t)npairs * p.I * 2;
+                const size_t row = (size_t)plan->slot_e[slot] * p.H + ch.r0;
+                const size_t s0 = row * (p.I / 32), s1 = s0 + (size_t)ch.n * (p.I / 32);
+                const size_t w0 = s0 & ~(size_t)15, w1 = (s1 + 15) & ~(size_t)15;
+                bulk_g2s(dst + off + hb, p.w2 + row * (p.I / CD), bc, bar, pol_w);
+                bulk_g2s(dst + off + hb + bc, p.s2 + w0, (uint32_t)(w1 - w0), bar, pol_w);
+                const void* hsrc = p.hr + (size_t)plan->slot_p0[slot] * p.I;
+                if (b2_done) {
+                    bulk_g2s(dst + off, hsrc, hb, bar, pol_h);
+                } else {
+                    const int q = plan->npend++;
+                    plan->pend_dst[q] = dst + off;
+                    plan->pend_src[q] = hsrc;
+                    plan->pend_bytes[q] = hb;
+                    plan->pend_bar[q] = bar;
+                    deferred = true;
+                }
+                off += down_seg_bytes<WFMT>(p, npairs, ch.n);
+            }
         } else {
             const int inter = ch.slot < 0 ? p.Is : p.I;
             const uint32_t hb = (uint32_t)ch.np * inter * 2;
@@ -1184,6 +1255,22 @@ struct Consumer {
     // (pair, row) result is written exactly once, unweighted, into ypair; the
     // weighted combine runs after the last chunk, in pair order.
     __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
+        if (WFMT != 0 && ch.kind == 6) {
+            // packed routed slots: each segment as a kind-2 chunk (its parts
+            // continue the round-robin over the warps)
+            uint32_t off = 0;
+            for (int k = 0; k < ch.np; ++k) {
+                const int slot = ch.slot + k;
+                const int npairs = plan->slot_p0[slot + 1] - plan->slot_p0[slot];
+                down_seg(Chunk{2, slot, ch.r0, ch.n, 0, npairs}, st + off);
+                off += down_seg_bytes<WFMT>(p, npairs, ch.n);
+            }
+            return;
+        }
+        down_seg(ch, st);
+    }
+
+    __device__ __forceinline__ void down_seg(const Chunk& ch, const uint8_t* st) {
         const int nparts = (ch.n + 3) >> 2;
         const int part0 = claim_rows(nparts);
         if (part0 >= nparts) return;

@@ -12,6 +12,7 @@ constexpr int consumer_warps(int) { return 11; }
 constexpr int block_threads(int wfmt) { return (consumer_warps(wfmt) + 1) * 32; }
 constexpr uint32_t kStageBytes = 32768;               // one ring stage
 constexpr int kMaxStages = 6;
+constexpr int kMaxPack = 4;  // routed slots' down rows in one MXFP4 / FP8 chunk
 constexpr int kMaxM = 16;
 constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
@@ -100,7 +101,9 @@ struct LayerParams {
 // A unit of the ring: the tiles one stage holds. kind 0 router rows, 1
 // gate/up rows, 2 down rows, 3 end of a phase (no data), 4 a split-K unit
 // (gate, up and transposed down rows), 5 gate/up rows laid out for the
-// tensor cores (rows at a padded pitch).
+// tensor cores (rows at a padded pitch), 6 the down rows of np consecutive
+// routed slots (MXFP4 / FP8), each slot a segment laid out as a kind-2 chunk
+// with all its pairs and the CTA's rows [r0, r0 + n).
 struct Chunk {
     int32_t kind;
     int32_t slot;    // -1 shared expert, else routed slot
@@ -137,8 +140,8 @@ struct Plan {
     uint32_t epoch;                 // this call's launch epoch
     // Activation copies of down chunks issued before grid barrier 2
     // (producer only): destination, barrier, bytes, source.
-    uint32_t pend_dst[kMaxStages], pend_bar[kMaxStages], pend_bytes[kMaxStages];
-    const void* pend_src[kMaxStages];
+    uint32_t pend_dst[kMaxStages * kMaxPack], pend_bar[kMaxStages * kMaxPack], pend_bytes[kMaxStages * kMaxPack];
+    const void* pend_src[kMaxStages * kMaxPack];
     int32_t npend;
 };
 
