@@ -869,6 +869,29 @@ __device__ __forceinline__ void dot4_mxh(const uint8_t* const (&crow)[4], const 
     }
 }
 
+// dot4_mxh with the activation blocks already converted: lane b (< nblk,
+// nblk <= 32) holds block b of each of the NT activations in a[t] (f16 times
+// 2^s) and 2^-s in inv[t].
+template <int NT>
+__device__ __forceinline__ void dot4_mxh_pre(const uint8_t* const (&crow)[4], const uint8_t* const (&srow)[4],
+                                             const uint4 (&a)[NT][4], const float (&inv)[NT], int nblk, int lane,
+                                             float (&acc)[4][NT]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[j][t] = 0.f;
+    if (lane < nblk) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t w[16];
+            decode_block(reinterpret_cast<const uint4*>(crow[j])[lane], w);
+            const float sw = e8m0_to_f32(srow[j][lane]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[j][t] = block_h(w, a[t]) * inv[t] * sw;
+        }
+    }
+}
+
 // ---- FP8 e4m3 with one fp32 scale per 128 elements of a row: codes
 // decoded to fp32 by the hardware conversion, products in fp32 through the
 // paired FMA (even and odd partial sums of each 8-code half); each 16-code
@@ -1254,6 +1277,66 @@ struct Consumer {
     // chunks resident together are worked on by all warps at once. Each
     // (pair, row) result is written exactly once, unweighted, into ypair; the
     // weighted combine runs after the last chunk, in pair order.
+    // MXFP4 routed down rows (I <= 1024: at most one 32-value block per
+    // lane): one warp takes the whole segment, converts each pair's
+    // activation block once (block_to_f16) and runs every four-row part of
+    // the segment against it, instead of one part per warp each converting
+    // the activations again (a third of the instructions of the part).
+    __device__ __forceinline__ void down_seg_mx(const Chunk& ch, const uint8_t* st, int nparts) {
+        if (claim_rows(1) != 0) return;
+        const int gbase = p.M + plan->slot_p0[ch.slot] + ch.p0;
+        const size_t s0 = ((size_t)plan->slot_e[ch.slot] * p.H + ch.r0) * (p.I / 32);
+        const size_t sofs = s0 - (s0 & ~(size_t)15);
+        const size_t hbytes = (size_t)ch.np * p.I * 2;
+        const uint8_t* codes = st + hbytes;
+        const uint8_t* scls = st + hbytes + (size_t)ch.n * (p.I / 2) + sofs;
+        const int nblk = p.I / 32;
+        const int bl = lane < nblk ? lane : 0;  // lanes past the blocks convert block 0 and add nothing
+        int q0 = 0;
+        for (; q0 + 2 <= ch.np; q0 += 2) {
+            uint4 a[2][4];
+            float inv[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                inv[t] = block_to_f16(reinterpret_cast<const uint4*>(st + (size_t)(q0 + t) * p.I * 2) + 4 * bl,
+                                      (bl >> 1) & 3, a[t]);
+            for (int part = 0; part < nparts; ++part) {
+                const int r = ch.r0 + 4 * part, nrow = min(4, ch.r0 + ch.n - r);
+                const uint8_t* crow[4];
+                const uint8_t* srow[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = 4 * part + min(jj, nrow - 1);
+                    crow[jj] = codes + (size_t)j * (p.I / 2);
+                    srow[jj] = scls + (size_t)j * nblk;
+                }
+                float acc[4][2];
+                dot4_mxh_pre<2>(crow, srow, a, inv, nblk, lane, acc);
+                reduce_store<2>(acc, nrow, ypair + (size_t)(gbase + q0) * p.rpc + (r - h0));
+            }
+        }
+        if (q0 < ch.np) {
+            uint4 a[1][4];
+            float inv[1];
+            inv[0] = block_to_f16(reinterpret_cast<const uint4*>(st + (size_t)q0 * p.I * 2) + 4 * bl, (bl >> 1) & 3,
+                                  a[0]);
+            for (int part = 0; part < nparts; ++part) {
+                const int r = ch.r0 + 4 * part, nrow = min(4, ch.r0 + ch.n - r);
+                const uint8_t* crow[4];
+                const uint8_t* srow[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = 4 * part + min(jj, nrow - 1);
+                    crow[jj] = codes + (size_t)j * (p.I / 2);
+                    srow[jj] = scls + (size_t)j * nblk;
+                }
+                float acc[4][1];
+                dot4_mxh_pre<1>(crow, srow, a, inv, nblk, lane, acc);
+                reduce_store<1>(acc, nrow, ypair + (size_t)(gbase + q0) * p.rpc + (r - h0));
+            }
+        }
+    }
+
     __device__ __forceinline__ void down(const Chunk& ch, const uint8_t* st) {
         if (WFMT != 0 && ch.kind == 6) {
             // packed routed slots: each segment as a kind-2 chunk (its parts
@@ -1272,6 +1355,10 @@ struct Consumer {
 
     __device__ __forceinline__ void down_seg(const Chunk& ch, const uint8_t* st) {
         const int nparts = (ch.n + 3) >> 2;
+        if (WFMT == 1 && ch.slot >= 0 && p.I <= 1024 && !(!MMA && p.htag)) {
+            down_seg_mx(ch, st, nparts);
+            return;
+        }
         const int part0 = claim_rows(nparts);
         if (part0 >= nparts) return;
         const bool shared = ch.slot < 0;
