@@ -2132,7 +2132,10 @@ __global__ void __launch_bounds__(block_threads(WFMT), 1) moe_layer_kernel(const
             }
             // the shared expert's tiles were fetched before routing finished;
             // computing them now overlaps the first routed tiles' latency
-            cs.qm = 0;
+            // one token: the first row goes to warp 1, so that the top-k warp
+            // (warp 0, busy ranking) owns none of the shared expert's rows
+            // and their stages free up without waiting for it
+            cs.qm = incremental ? 1 : 0;
             if (ok) ok = cs.consume_phase();  // shared, then routed gate/up
             named_bar_sync(1, NCT);  // this CTA's activations are stored
             if (tid == 0) trace_mark(p, 6);
