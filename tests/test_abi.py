@@ -46,7 +46,10 @@ def test_workspace_bytes_and_shape_checks(api):
     assert 0 < n2 < n16
     assert n16 >= 1024 + 16 * 512 * 4 + 16 * 768 * 2 + 16 * 8 * 768 * 2
     # one token: room for the split-K layer's partial outputs (MOE_MAX_GRID x H fp32)
-    assert n1 >= 256 * 2560 * 4
+    # and for the tagged activations (32-bit words, shared expert + k routed pairs)
+    assert n1 >= 1024 + 512 * 8 + 256 * 2560 * 4 + (768 + 8 * 768) * 4
+    mx1 = api.workspace_bytes(api.make_shape(2560, 512, 8, 768, 768, 1), 1)
+    assert 0 < mx1 < n1  # MXFP4 one-token layers keep grid barrier 2: no tagged words
     assert api.workspace_bytes(ling, 0) == 0
     assert api.workspace_bytes(ling, 17) == 0
     for bad in (api.make_shape(2500, 512, 8, 768, 768),   # H not a multiple of 256
