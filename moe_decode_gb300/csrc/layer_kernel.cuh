@@ -16,6 +16,8 @@
 //            are claimed chunk by chunk from a global counter;
 //            h = silu(W1 x) * (W3 x) goes to the workspace in bf16.
 //                                                       -> grid barrier 2
+//            (one-token bf16 launches: no barrier; h goes out as tagged
+//            words that ride with the down chunks' copies)
 //   phase 2  down projection + weighted combine: CTA c owns output rows
 //            [cH/G, (c+1)H/G); each (token, expert) pair's down result is
 //            kept unweighted in shared memory, then y = shared expert +
@@ -248,8 +250,8 @@ __device__ __forceinline__ bool grid_wait(const unsigned* ctr, unsigned target, 
 }
 
 // ------------------------------------------------------------ call counters
-// Grid barrier 2 and the routed gate/up work counter of the call with this
-// epoch (two sets, by parity).
+// Grid barrier 2, the routed gate/up work counter and the entry counter of
+// the call with this epoch (two sets, by parity).
 __device__ __forceinline__ unsigned* ctl_bar2(const LayerParams& p, uint32_t epoch) {
     return p.ctrl + ((epoch & 1u) ? kCtlBar2Odd : kCtlBar2);
 }
@@ -302,7 +304,8 @@ struct Ring {
 // One elected lane. Weight tiles of a chunk are issued as soon as its stage
 // is free; the activation tiles of a down chunk are produced by all CTAs and
 // may only be fetched after grid barrier 2, so until then they wait in a
-// short list in shared memory.
+// short list in shared memory (one-token bf16 launches copy tagged
+// activations at once instead).
 template <int WFMT, bool PAD = false>
 struct Producer {
     const LayerParams& p;
@@ -312,7 +315,7 @@ struct Producer {
     uint64_t pol_h;  // activations: keep
     bool b2_done;
     uint32_t complete_upto;  // chunks whose copies were all issued
-    uint32_t epoch;          // this call's epoch (read after the dependency wait)
+    uint32_t epoch;          // this call's epoch (from the plan, once it is published)
 
     __device__ __forceinline__ void flush_pending() {
         for (int i = 0; i < plan->npend; ++i)
